@@ -1,0 +1,121 @@
+"""Seeded synthetic inputs for the fused MoE layer.
+
+This module is shared by the CUDA path's tests/benchmark and by the CPU oracle's
+tests. It holds input generation only: no step of the MoE computation lives here.
+
+Recipe (all configs):
+  * ``numpy.random.default_rng(seed)`` (PCG64), float32 standard normals, drawn
+    in this order: hidden, router_w, w_gate_up, w_down, then (skewed sweep
+    only) the expert-rank permutation of the Zipf logit bias.
+  * Each tensor is scaled by its standard deviation in float32 and rounded
+    once to bf16 (round to nearest, ties to even); both sides then read the
+    same bf16 bit patterns, carried as ``uint16`` arrays.
+  * Layouts follow the stacked-expert packing of the weight loader described
+    on "模型与权重加载" (streaming loader, step 4): ``w_gate_up[E, 2I, H]`` with
+    gate rows first, ``w_down[E, H, I]``.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+
+@dataclasses.dataclass(frozen=True)
+class MoEShape:
+    name: str
+    T: int
+    H: int
+    E: int
+    top_k: int
+    I: int
+    renorm: bool
+    w_std: float = 0.02
+    router_std: Optional[float] = None  # defaults to w_std
+    x_std: float = 1.0
+    zipf_s: Optional[float] = None      # per-expert logit bias drawn for a Zipf load
+    seed: int = 0
+
+    def with_T(self, T: int) -> "MoEShape":
+        return dataclasses.replace(self, T=T, name=f"{self.name}_T{T}")
+
+
+# The workloads: a tiny parity case, the Qwen3-30B-A3B-shaped decode and
+# prefill layers, the Qwen3-235B-A22B-shaped large prefill layer and the
+# skewed-load sweep (one shape per T).
+TINY = MoEShape("tiny", T=16, H=128, E=8, top_k=2, I=64, renorm=True)
+DECODE = MoEShape("decode_qwen3_30b_a3b", T=64, H=2048, E=128, top_k=8, I=768, renorm=True)
+PREFILL = MoEShape("prefill_qwen3_30b_a3b", T=4096, H=2048, E=128, top_k=8, I=768, renorm=True)
+LARGE = MoEShape("prefill_qwen3_235b_a22b", T=8192, H=4096, E=128, top_k=8, I=1536,
+                 renorm=True, w_std=0.015, router_std=0.015)
+SWEEP_T = (1, 8, 32, 128, 512, 2048, 16384)
+SWEEP = MoEShape("zipf_sweep", T=1, H=2048, E=128, top_k=8, I=768, renorm=False, zipf_s=1.1)
+WORKLOADS = {s.name: s for s in (TINY, DECODE, PREFILL, LARGE)}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Input generation only (the values are finite normals)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    b = b + (np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1)))
+    return (b >> np.uint32(16)).astype(np.uint16)
+
+
+def _normal_bf16(rng: np.random.Generator, shape, std: float, chunk: int = 1 << 24) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        m = min(chunk, n - s)
+        v = rng.standard_normal(m, dtype=np.float32)
+        if std != 1.0:
+            v *= np.float32(std)
+        out[s:s + m] = f32_to_bf16_bits(v)
+    return out.reshape(shape)
+
+
+def zipf_logit_bias(E: int, s: float, perm: np.ndarray) -> np.ndarray:
+    """bias[e] = ln(q_rank(e)) with q_r proportional to r^-s over ranks 1..E.
+
+    Expert e gets rank perm[e]+1. A logit bias of ln(q) multiplies that expert's
+    unnormalised softmax mass by q, which skews the router's load towards a
+    Zipf(s) profile (the top experts saturate at one row per token)."""
+    r = np.arange(1, E + 1, dtype=np.float64)
+    q = r ** (-s)
+    q /= q.sum()
+    return np.log(q[perm]).astype(np.float32)
+
+
+def make_inputs(shape: MoEShape, weights: bool = True) -> dict:
+    """Draw the inputs of one MoE layer call. Returns a dict of numpy arrays:
+    hidden[T,H], router_w[E,H], w_gate_up[E,2I,H], w_down[E,H,I] (uint16 bf16
+    bits) and router_bias[E] (float32, or None)."""
+    rng = np.random.default_rng(shape.seed)
+    T, H, E, I = shape.T, shape.H, shape.E, shape.I
+    rstd = shape.router_std if shape.router_std is not None else shape.w_std
+    d = {"hidden": _normal_bf16(rng, (T, H), shape.x_std),
+         "router_w": _normal_bf16(rng, (E, H), rstd)}
+    if weights:
+        d["w_gate_up"] = _normal_bf16(rng, (E, 2 * I, H), shape.w_std)
+        d["w_down"] = _normal_bf16(rng, (E, H, I), shape.w_std)
+    d["router_bias"] = None
+    if shape.zipf_s is not None:
+        perm = rng.permutation(E)
+        d["router_bias"] = zipf_logit_bias(E, shape.zipf_s, perm)
+    return d
+
+
+def random_small_inputs(seed: int, T: int, H: int, E: int, I: int,
+                        x_std: float = 1.0, w_std: float = 0.1,
+                        bias: bool = False) -> dict:
+    """Small random cases for property tests (same recipe, free shapes)."""
+    rng = np.random.default_rng(seed)
+    d = {"hidden": _normal_bf16(rng, (T, H), x_std),
+         "router_w": _normal_bf16(rng, (E, H), w_std),
+         "w_gate_up": _normal_bf16(rng, (E, 2 * I, H), w_std),
+         "w_down": _normal_bf16(rng, (E, H, I), w_std),
+         "router_bias": None}
+    if bias:
+        d["router_bias"] = rng.standard_normal(E, dtype=np.float32)
+    return d
