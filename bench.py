@@ -1,0 +1,376 @@
+"""Throughput of the fused MoE layer on GB300, one JSON line per run.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mm|reference]
+                    [--workload decode_qwen3_30b_a3b|prefill_qwen3_30b_a3b|...]
+
+A step is one pass of the whole layer (route, align, gather, gate_up GEMM +
+SiLU*up, down GEMM + weighted scatter-add, rounding) over one synthetic batch.
+The default workload is the Qwen3-30B-A3B-shaped decode layer (T=64, H=2048,
+E=128, k=8, I=768): every step streams the selected experts' weights (about
+1.2 GB, far above the 129 MB L2) from HBM, so no L2 flush is needed.
+
+--impl reference times the CPU oracle on the host cores instead (a baseline,
+not a target). Under torchrun every rank runs its own replica (the layer
+shards by tokens with no exchange), and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+_CORES = os.cpu_count() or 1
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_layer_mm_gb300 import synthetic  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (Qwen3-30B-A3B shape) + % of BF16 TC / HBM roofline"
+UNIT = "tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["mixture_experts_layer_mm_gb300/csrc/gemm.cu",
+                  "mixture_experts_layer_mm_gb300/csrc/mm_device.cuh"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], 0.0, set()
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_work(shape, ids: np.ndarray):
+    """Algorithmic bytes / flops of the layer and of its two GEMM kernels for
+    one step, from the realised routing (padding, re-reads and the fp32
+    accumulator round trip excluded)."""
+    T, H, E, k, I = shape.T, shape.H, shape.E, shape.top_k, shape.I
+    D = int(np.unique(ids).size)          # distinct experts selected in the batch
+    M = T * k                             # real (token, expert) rows
+    gu_bytes = D * 2 * I * H * 2 + T * H * 2 + M * I * 2
+    dn_bytes = D * H * I * 2 + M * I * 2 + T * H * 4
+    layer_bytes = D * 3 * H * I * 2 + E * H * 2 + 2 * T * H * 2
+    return {"D": D,
+            "gate_up": {"bytes": gu_bytes, "flops": 2 * M * H * 2 * I},
+            "down": {"bytes": dn_bytes, "flops": 2 * M * I * H},
+            "layer": {"bytes": layer_bytes, "flops": 2 * T * E * H + 2 * M * 3 * H * I}}
+
+
+def load_traffic(workload: str, kernel: str):
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    d = json.load(open(TRAFFIC_FILE))
+    ent = d.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None  # counters were taken on another version of the kernel
+    return ent.get("bytes_per_launch")
+
+
+def run_reference(args, shape, ws, rank):
+    """The CPU oracle on the host cores, on a bounded sample of the workload."""
+    if rank != 0:
+        return
+    from oracle import moe_oracle as O
+    d = synthetic.make_inputs(shape)
+    n_tok = min(shape.T, args.ref_tokens)
+    sub = dict(d)
+    sub["hidden"] = d["hidden"][:n_tok]
+
+    def step():
+        O.moe_layer(sub, shape.top_k, shape.renorm)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    v = n_tok * args.steps / dt
+    sample = (f"first {n_tok} of the {shape.T} tokens of {shape.name} per step, "
+              f"full routing + grouping + fp32 expert loop")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E,
+                       "top_k": shape.top_k, "I": shape.I, "renorm": shape.renorm,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(shape, budget_s: float):
+    """Times the oracle as it stands on a bounded sample (about budget_s)."""
+    from oracle import moe_oracle as O
+    d = synthetic.make_inputs(shape)
+    n_tok = min(shape.T, 64)
+    sub = dict(d)
+    sub["hidden"] = d["hidden"][:n_tok]
+    t0 = time.perf_counter()
+    O.moe_layer(sub, shape.top_k, shape.renorm)
+    one = time.perf_counter() - t0
+    reps = max(1, min(20, int(budget_s / max(one, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        O.moe_layer(sub, shape.top_k, shape.renorm)
+    dt = time.perf_counter() - t0
+    return {"value": n_tok * reps / dt, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+            "kind": "oracle",
+            "sample": f"{reps} oracle passes over the first {n_tok} tokens of {shape.name} "
+                      f"({dt:.1f} s, numpy fp32 with OpenBLAS threads)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mm", "reference"], default="mm")
+    ap.add_argument("--workload", default=synthetic.DECODE.name)
+    ap.add_argument("--sweep-T", type=int, default=None, help="run the Zipf sweep shape at this T")
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    ws, rank, local = dist_info()
+    shape = synthetic.SWEEP.with_T(args.sweep_T) if args.sweep_T else synthetic.WORKLOADS[args.workload]
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    if args.impl == "reference":
+        run_reference(args, shape, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    import mixture_experts_layer_mm_gb300 as mm
+    mm.lib()  # fails loudly if the CUDA library is missing
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    # Each replica gets its own batch (hidden seed = rank); the layer weights are shared.
+    w = synthetic.make_weights(shape)
+    hid_np = synthetic.make_hidden(synthetic.MoEShape(**{**shape.__dict__, "seed": rank}))
+    bias_np = synthetic.make_router_bias(shape)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    router_w, w_gu, w_dn = to_dev(w["router_w"]), to_dev(w["w_gate_up"]), to_dev(w["w_down"])
+    del w
+    hidden = to_dev(hid_np)
+    bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+    k, renorm = shape.top_k, shape.renorm
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        mm.mm_moe_forward(hidden, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    st = mm.mm_poll_device_status()
+    if st != mm.MM_OK:
+        raise RuntimeError(f"device status after warm-up: {mm.status_string(st)}")
+    ids, _ = mm.mm_route(hidden, router_w, k, renorm, router_bias=bias)
+    work = algorithmic_work(shape, ids.cpu().numpy())
+
+    # ---- timed region A: the layer as a user calls it (device-resident inputs)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            fwd()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms)
+    clocks = clk.summary()
+
+    # ---- timed region B: same steps, stage events recorded around each kernel
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mm.PROFILE_STAGES) + 1)]
+           for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        mm.mm_moe_forward_profiled(hidden, router_w, w_gu, w_dn, k, renorm, evs[i], out=out,
+                                   router_bias=bias)
+    torch.cuda.synchronize()
+    barrier()
+    stage_ms = {}
+    for j, name in enumerate(mm.PROFILE_STAGES):
+        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                         for i in range(args.steps))
+
+    # ---- timed region C: end to end from pinned host memory through the C ABI
+    h_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
+    h_host.copy_(hidden.cpu())
+    o_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
+    h_dev = torch.empty_like(hidden)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        mm.mm_moe_forward(h_dev, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
+        o_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps)
+    st = mm.mm_poll_device_status()
+    if st != mm.MM_OK:
+        raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
+
+    pk, pk_kind = peaks()
+    T_all = shape.T * ws
+    value = T_all / (ms * 1e-3)
+    # The dominant kernel: the gate_up grouped GEMM (largest share of bytes and flops).
+    dom = "gate_up"
+    dom_ms = stage_ms[dom]
+    if shape.T * k <= 2048:   # few rows per expert: bound by streaming the weights
+        achieved = work[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"],
+                "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)"}
+    else:
+        achieved = work[dom]["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "peak_kind": f"{pk_kind} bf16_tflops (burst)"}
+    roof["kernel"] = f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
+    roof["traffic"] = load_traffic(shape.name, dom)
+    layer_ms = sum(stage_ms.values())
+    roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+    launches_per_step = 6 if shape.T <= 1024 else 8
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded normals, bf16; random-init weights of the named shape)",
+            "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E,
+                       "top_k": k, "I": shape.I, "renorm": renorm,
+                       "distinct_experts": work["D"], "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2: each step streams the selected experts' "
+                             f"weights ({work['layer']['bytes'] / 1e9:.2f} GB)"},
+            "roofline": roof,
+            "stage_ms": {n: round(v, 5) for n, v in stage_ms.items()},
+            "stage_sum_ms": layer_ms,
+            "e2e": {"value": T_all / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": int(h_host.numel() * 2),
+                    "d2h_bytes_per_step": int(o_host.numel() * 2)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(shape, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * mm.h — C ABI of a fused Mixture-of-Experts layer for one GB300 (sm_103a).
+ *
+ * The layer is the Qwen3-MoE feed-forward block: for each token a router
+ * linear gives one logit per expert, a softmax over all experts turns them
+ * into scores, the k best experts are kept (optionally renormalised), each
+ * kept expert runs a SwiGLU MLP (gate_up projection, SiLU(gate) * up, down
+ * projection) and the expert outputs are summed weighted by their scores.
+ * Sources: "mini-sglang guide, chapter 7" (paragraphs on layers/moe.py and
+ * moe/fused.py), "The op layer: BaseOP and the layers" (Linear layers table:
+ * the router is a replicated linear), "模型与权重加载" (ModelConfig MoE
+ * fields; GatedMLP; streaming loader, step 4: experts stacked into [E, ...]).
+ *
+ * Conventions for every entry point:
+ *   - Pointer arguments are DEVICE pointers on the current CUDA device unless
+ *     marked host. They are owned by the caller, must be contiguous row-major,
+ *     16-byte aligned, and must not alias one another.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous on that stream and never synchronises the host,
+ *     except mm_poll_device_status and the first call on a device (which
+ *     allocates the library's state there).
+ *   - Errors are returned, never raised: arguments are checked before any
+ *     launch, and on error no output is written. Device-side faults that a
+ *     kernel can detect (an expert id out of range, a wait that timed out)
+ *     are recorded in a per-device status word read by
+ *     mm_poll_device_status; kernels never trap.
+ *   - Supported shapes: T >= 0, 1 <= E <= 256, 1 <= top_k <= min(E, 32),
+ *     H and I multiples of 64, T*top_k < 2^31. Anything else returns
+ *     MM_ERR_UNSUPPORTED (or MM_ERR_INVALID_ARG for values that make no sense).
+ */
+#ifndef MM_H
+#define MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, misaligned pointer */
+  MM_ERR_UNSUPPORTED = 2,   /* valid but outside the supported shapes */
+  MM_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  MM_ERR_NO_MEMORY = 4,     /* workspace allocation failed or too small */
+  MM_ERR_DEVICE = 5,        /* a kernel flagged bad input (e.g. expert id out of range) */
+  MM_ERR_TIMEOUT = 6        /* a kernel's bounded wait ran out and it returned early */
+} mm_status;
+
+/* Gemm modes of mm_grouped_gemm. */
+enum { MM_GEMM_GATE_UP = 0, MM_GEMM_DOWN = 1 };
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* mm_status_string(int status);
+
+/*
+ * Routing: router logits, softmax over all E experts, top-k, weights.
+ * ("mini-sglang guide, chapter 7", layers/moe.py; "模型与权重加载",
+ * ModelConfig: num_experts = E, num_experts_per_tok = top_k, norm_topk_prob.)
+ *
+ *   logit[t,e]   = sum_h hidden[t,h] * router_w[e,h] (+ router_bias[e]),
+ *                  bf16 products accumulated in fp32
+ *   p[t,e]       = softmax over all E of logit[t,:]
+ *   topk_ids[t,:]= the top_k experts with the largest logit (equal logits: the
+ *                  lower id wins), written in ASCENDING expert order
+ *   topk_w[t,j]  = p[t, topk_ids[t,j]]; if renorm != 0, divided by the sum
+ *                  of the selected p (norm_topk_prob)
+ *
+ * hidden [T,H] bf16, router_w [E,H] bf16, router_bias [E] fp32 or NULL;
+ * outputs topk_ids [T,top_k] int32, topk_w [T,top_k] fp32.
+ * T == 0 is a no-op.
+ */
+int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
+             int T, int H, int E, int top_k, int renorm,
+             int32_t* topk_ids, float* topk_w, void* stream);
+
+/*
+ * Length of the sorted_token_ids buffer mm_align needs: T*top_k +
+ * E*(block_m-1) (each expert wastes fewer than block_m padding slots).
+ * Returns -1 for invalid arguments. Host-only, no CUDA call.
+ */
+int64_t mm_align_capacity(int T, int top_k, int E, int block_m);
+
+/*
+ * Token batching by expert ("mini-sglang guide, chapter 7", moe/fused.py:
+ * tokens are grouped by their assigned expert so each expert's weights are
+ * read once with coalesced accesses).
+ *
+ * A stable counting sort of the flat assignment ids f = t*top_k + j by
+ * expert id topk_ids[f]. Expert e owns slots [expert_offsets[e],
+ * expert_offsets[e+1]) of sorted_token_ids: its assignments in increasing f,
+ * then padding entries equal to T*top_k up to a multiple of block_m. Experts
+ * without assignments own no slots. expert_offsets[E] is the padded total;
+ * slots from there up to mm_align_capacity() hold T*top_k as well.
+ *
+ * topk_ids [T,top_k] int32 (each row: distinct ids in [0,E)); outputs
+ * sorted_token_ids [mm_align_capacity()] int32, expert_offsets [E+1] int32,
+ * expert_counts [E] int32 or NULL. 1 <= block_m <= 256. Ids outside [0,E) or
+ * repeated within a row are dropped and flag MM_ERR_DEVICE in the device
+ * status. For T > 1024 the library's internal workspace holds per-block
+ * counts, so calls on one device must not overlap; the result is
+ * deterministic (bit-identical on every call).
+ */
+int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+             int32_t* sorted_token_ids, int32_t* expert_offsets, int32_t* expert_counts,
+             void* stream);
+
+/*
+ * One grouped GEMM over the expert segments that mm_align produced, on the
+ * 5th-generation tensor cores (bf16 operands, fp32 accumulation in tensor
+ * memory). For every expert e and every slot r in its segment:
+ *
+ * mode MM_GEMM_GATE_UP ("模型与权重加载", GatedMLP: gate_up_proj then
+ *   silu_and_mul; rows [0,N) of each expert's matrix are gate, [N,2N) up):
+ *     A = hidden [T,K] bf16, row r reads token sorted_token_ids[r] / top_k
+ *         (padding rows read zeros)
+ *     B = w_gate_up [E, 2N, K] bf16
+ *     C = act [capacity, N] bf16:  act[r,n] = silu(g) * u,
+ *         g = A_r . B[e,n,:], u = A_r . B[e,N+n,:]   (fp32, one bf16 rounding)
+ *     topk_w unused (may be NULL).
+ * mode MM_GEMM_DOWN ("模型与权重加载", GatedMLP: down_proj; "mini-sglang
+ *   guide, chapter 7": expert outputs weighted by their scores and summed):
+ *     A = act [capacity, K] bf16, B = w_down [E, N, K] bf16,
+ *     C = acc [T, N] fp32:  acc[f / top_k, n] += topk_w[f] * (A_r . B[e,n,:])
+ *         for every real slot (f = sorted_token_ids[r] < T*top_k), by atomic
+ *         fp32 adds (summation order is not fixed). The caller zeroes acc.
+ *
+ * capacity = mm_align_capacity(T, top_k, E, block_m). Gate-up mode stages the
+ * gathered rows in the library's internal workspace (calls on one device must
+ * not overlap). N and K multiples of 64.
+ */
+int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
+                    const int32_t* sorted_token_ids, const int32_t* expert_offsets,
+                    const float* topk_w, int T, int top_k, int E, int N, int K, int block_m,
+                    void* stream);
+
+/*
+ * The whole MoE layer: route, align, gate_up GEMM + SiLU*up, down GEMM +
+ * weighted scatter-add, and the fp32 -> bf16 rounding of the sum.
+ *
+ * hidden [T,H] bf16, router_w [E,H] bf16, w_gate_up [E,2I,H] bf16 (gate rows
+ * first), w_down [E,H,I] bf16; out [T,H] bf16. Uses the library's internal
+ * per-device workspace (grown on demand with cudaMalloc, which synchronises
+ * the device the first time a larger size is needed); calls on one device
+ * must therefore not overlap. T == 0 is a no-op.
+ */
+int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w,
+                   const uint16_t* w_gate_up, const uint16_t* w_down,
+                   int T, int H, int E, int I, int top_k, int renorm,
+                   uint16_t* out, void* stream);
+
+/* Bytes of workspace mm_moe_forward_ex needs for these sizes (-1 if invalid). */
+int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k);
+
+/*
+ * mm_moe_forward with an optional router bias (fp32 [E] added to the
+ * logits, NULL for none) and an optional caller workspace: if `workspace` is
+ * non-NULL it must hold at least mm_moe_workspace_size() bytes (256-byte
+ * aligned) and the call allocates nothing; calls with distinct workspaces may
+ * run concurrently. If `workspace` is NULL the internal workspace is used.
+ */
+int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w,
+                      const float* router_bias,
+                      const uint16_t* w_gate_up, const uint16_t* w_down,
+                      int T, int H, int E, int I, int top_k, int renorm,
+                      uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Stage timing of mm_moe_forward_ex, for profiling. Same arguments, plus
+ * `events`: a host array of MM_PROFILE_EVENTS cudaEvent_t handles (created
+ * by the caller with timing enabled). events[i] is recorded on `stream`
+ * before stage i and events[6] after the last one; the stages are
+ * 0 route, 1 align, 2 gather of token rows, 3 gate_up GEMM, 4 down GEMM,
+ * 5 fp32 -> bf16 rounding. No stage is skipped or changed; nothing is
+ * synchronised. (Measurement support: the pages describe no counterpart.)
+ */
+#define MM_PROFILE_EVENTS 7
+int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,
+                            const float* router_bias,
+                            const uint16_t* w_gate_up, const uint16_t* w_down,
+                            int T, int H, int E, int I, int top_k, int renorm,
+                            uint16_t* out, void* workspace, size_t workspace_bytes, void* stream,
+                            void* const* events);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns MM_OK, MM_ERR_DEVICE (bad ids seen), MM_ERR_TIMEOUT (a kernel
+ * gave up waiting and returned early; its outputs are undefined) or
+ * MM_ERR_CUDA.
+ */
+int mm_poll_device_status(void* stream);
+
+/* Frees the internal workspaces of every device. Not thread-safe with calls in flight. */
+void mm_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MM_H */

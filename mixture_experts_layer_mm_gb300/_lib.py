@@ -1,0 +1,235 @@
+"""Thin ctypes binding of the C ABI in include/mm.h.
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the MoE layer runs in libmm.so's kernels.
+There is no fallback: if the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmm.so")
+
+MM_OK = 0
+MM_ERR_INVALID_ARG = 1
+MM_ERR_UNSUPPORTED = 2
+MM_ERR_CUDA = 3
+MM_ERR_NO_MEMORY = 4
+MM_ERR_DEVICE = 5
+MM_ERR_TIMEOUT = 6
+MM_GEMM_GATE_UP = 0
+MM_GEMM_DOWN = 1
+FORWARD_BLOCK_M = 16  # expert segments are padded to this multiple by mm_moe_forward
+
+# Every entry point include/mm.h declares, with its ctypes signature.
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "mm_status_string": (ctypes.c_char_p, [_I]),
+    "mm_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "mm_align_capacity": (_I64, [_I, _I, _I, _I]),
+    "mm_align": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "mm_grouped_gemm": (_I, [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "mm_moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "mm_moe_workspace_size": (_I64, [_I, _I, _I, _I, _I]),
+    "mm_moe_forward_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mm_moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
+                                     _P]),
+    "mm_poll_device_status": (_I, [_P]),
+    "mm_shutdown": (None, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class MMError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmm.so (built by __graft_entry__.build()); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run __graft_entry__.build())")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().mm_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> None:
+    if code != MM_OK:
+        raise MMError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype: torch.dtype, name: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def mm_align_capacity(T: int, top_k: int, E: int, block_m: int) -> int:
+    return int(lib().mm_align_capacity(T, top_k, E, block_m))
+
+
+def mm_moe_workspace_size(T: int, H: int, E: int, I: int, top_k: int) -> int:
+    return int(lib().mm_moe_workspace_size(T, H, E, I, top_k))
+
+
+def mm_route(hidden, router_w, top_k: int, renorm: bool, router_bias=None,
+             topk_ids=None, topk_w=None, stream=None):
+    """Router + softmax + top-k. Returns (topk_ids int32 [T,k], topk_w fp32 [T,k])."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    if topk_ids is None:
+        topk_ids = torch.empty((T, top_k), dtype=torch.int32, device=hidden.device)
+    if topk_w is None:
+        topk_w = torch.empty((T, top_k), dtype=torch.float32, device=hidden.device)
+    _check(lib().mm_route(_ptr(hidden, torch.bfloat16, "hidden"),
+                          _ptr(router_w, torch.bfloat16, "router_w"),
+                          _ptr(router_bias, torch.float32, "router_bias"),
+                          T, H, E, top_k, int(bool(renorm)),
+                          _ptr(topk_ids, torch.int32, "topk_ids"),
+                          _ptr(topk_w, torch.float32, "topk_w"), _stream(stream)), "mm_route")
+    return topk_ids, topk_w
+
+
+def mm_align(topk_ids, E: int, block_m: int, sorted_token_ids=None, expert_offsets=None,
+             expert_counts=None, stream=None):
+    """Block-padded grouping by expert. Returns (sorted_token_ids, expert_offsets, expert_counts)."""
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    cap = mm_align_capacity(T, k, E, block_m)
+    if cap < 0:
+        raise MMError(MM_ERR_INVALID_ARG, "mm_align_capacity")
+    if sorted_token_ids is None:
+        sorted_token_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    if expert_offsets is None:
+        expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    if expert_counts is None:
+        expert_counts = torch.empty(E, dtype=torch.int32, device=dev)
+    _check(lib().mm_align(_ptr(topk_ids, torch.int32, "topk_ids"), T, k, E, block_m,
+                          _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                          _ptr(expert_offsets, torch.int32, "expert_offsets"),
+                          _ptr(expert_counts, torch.int32, "expert_counts"),
+                          _stream(stream)), "mm_align")
+    return sorted_token_ids, expert_offsets, expert_counts
+
+
+def mm_grouped_gemm(mode: int, A, B, C, sorted_token_ids, expert_offsets, topk_w,
+                    T: int, top_k: int, block_m: int, stream=None):
+    """One grouped GEMM (MM_GEMM_GATE_UP or MM_GEMM_DOWN); C is written in place."""
+    E = B.shape[0]
+    if mode == MM_GEMM_GATE_UP:
+        N, K = B.shape[1] // 2, B.shape[2]
+        cdt = torch.bfloat16
+    else:
+        N, K = B.shape[1], B.shape[2]
+        cdt = torch.float32
+    _check(lib().mm_grouped_gemm(mode, _ptr(A, torch.bfloat16, "A"), _ptr(B, torch.bfloat16, "B"),
+                                 _ptr(C, cdt, "C"),
+                                 _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                                 _ptr(expert_offsets, torch.int32, "expert_offsets"),
+                                 _ptr(topk_w, torch.float32, "topk_w"),
+                                 T, top_k, E, N, K, block_m, _stream(stream)), "mm_grouped_gemm")
+    return C
+
+
+def mm_moe_forward(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool,
+                   out=None, router_bias=None, workspace=None, stream=None):
+    """The whole MoE layer; returns out [T, H] bf16."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    if router_bias is None and workspace is None:
+        _check(lib().mm_moe_forward(_ptr(hidden, torch.bfloat16, "hidden"),
+                                    _ptr(router_w, torch.bfloat16, "router_w"),
+                                    _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+                                    _ptr(w_down, torch.bfloat16, "w_down"),
+                                    T, H, E, I, top_k, int(bool(renorm)),
+                                    _ptr(out, torch.bfloat16, "out"), _stream(stream)),
+               "mm_moe_forward")
+        return out
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().mm_moe_forward_ex(_ptr(hidden, torch.bfloat16, "hidden"),
+                                   _ptr(router_w, torch.bfloat16, "router_w"),
+                                   _ptr(router_bias, torch.float32, "router_bias"),
+                                   _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+                                   _ptr(w_down, torch.bfloat16, "w_down"),
+                                   T, H, E, I, top_k, int(bool(renorm)),
+                                   _ptr(out, torch.bfloat16, "out"), ws_ptr, ws_bytes,
+                                   _stream(stream)), "mm_moe_forward_ex")
+    return out
+
+
+PROFILE_STAGES = ("route", "align", "gather", "gate_up", "down", "finalize")
+
+
+def mm_moe_forward_profiled(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool,
+                            events, out=None, router_bias=None, workspace=None, stream=None):
+    """mm_moe_forward that records 7 torch.cuda.Event (timing enabled) around
+    its stages (PROFILE_STAGES) on the stream; returns out."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if len(events) != len(PROFILE_STAGES) + 1:
+        raise ValueError("need 7 events")
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib().mm_moe_forward_profiled(_ptr(hidden, torch.bfloat16, "hidden"),
+                                         _ptr(router_w, torch.bfloat16, "router_w"),
+                                         _ptr(router_bias, torch.float32, "router_bias"),
+                                         _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+                                         _ptr(w_down, torch.bfloat16, "w_down"),
+                                         T, H, E, I, top_k, int(bool(renorm)),
+                                         _ptr(out, torch.bfloat16, "out"), ws_ptr, ws_bytes,
+                                         _stream(stream), ev), "mm_moe_forward_profiled")
+    return out
+
+
+def mm_poll_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(lib().mm_poll_device_status(_stream(stream)))
+
+
+def mm_shutdown() -> None:
+    lib().mm_shutdown()

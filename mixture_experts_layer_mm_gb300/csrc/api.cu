@@ -1,0 +1,342 @@
+// The C ABI of include/mm.h: argument checks, the per-device state
+// (SM count, status word, internal workspace) and the launch sequence of the
+// MoE layer. Every computing step runs in the kernels of route.cu, align.cu
+// and gemm.cu; this file only validates, lays out memory and launches.
+#include <mutex>
+
+#include "mm.h"
+#include "mm_device.cuh"
+#include "mm_internal.h"
+
+namespace {
+
+using namespace mm;
+
+// Per-device status word (each device that loads the module has its own copy).
+__device__ unsigned g_status_word;
+
+struct DevState {
+  bool init = false;
+  int sms = 0;
+  unsigned* status = nullptr;  // device address of g_status_word
+  void* ws = nullptr;          // internal workspace
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Requires g_mu held.
+int device_state(DevState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MM_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MM_ERR_UNSUPPORTED;
+  DevState& s = g_dev[dev];
+  if (!s.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MM_ERR_CUDA;
+    if (major != 10 || minor != 3) return MM_ERR_UNSUPPORTED;  // built for sm_103a only
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.status), g_status_word) != cudaSuccess)
+      return MM_ERR_CUDA;
+    s.init = true;
+  }
+  *out = &s;
+  return MM_OK;
+}
+
+// Grows the internal workspace to at least `bytes`. Requires g_mu held.
+int ensure_ws(DevState* s, size_t bytes) {
+  if (s->ws_bytes >= bytes) return MM_OK;
+  if (s->ws != nullptr) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return MM_ERR_CUDA;  // work may still use it
+    cudaFree(s->ws);
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+  }
+  const size_t b = bytes + bytes / 8 + 4096;
+  if (cudaMalloc(&s->ws, b) != cudaSuccess) {
+    cudaGetLastError();
+    s->ws = nullptr;
+    return MM_ERR_NO_MEMORY;
+  }
+  s->ws_bytes = b;
+  return MM_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MM_OK : MM_ERR_CUDA; }
+
+int check_route_shape(int T, int H, int E, int top_k) {
+  if (T < 0 || H <= 0 || E <= 0 || top_k <= 0) return MM_ERR_INVALID_ARG;
+  if (E > kMaxExperts || top_k > kMaxTopK || top_k > E || H % 64 != 0) return MM_ERR_UNSUPPORTED;
+  if ((long long)T * top_k >= (1LL << 31) || (long long)T * H >= (1LL << 40))
+    return MM_ERR_UNSUPPORTED;
+  return MM_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct ForwardLayout {
+  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
+  long long capacity;
+};
+
+ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
+  ForwardLayout L;
+  L.capacity = (long long)T * k + (long long)E * (kForwardBlockM - 1);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += round256(bytes);
+    return o;
+  };
+  L.ids = take((size_t)T * k * 4);
+  L.w = take((size_t)T * k * 4);
+  L.sorted = take((size_t)L.capacity * 4);
+  L.offsets = take((size_t)(E + 1) * 4);
+  L.counts = take((size_t)E * 4);
+  L.scratch = take((size_t)align_scratch_ints(T, E) * 4);
+  L.xs = take((size_t)L.capacity * H * 2);
+  L.act = take((size_t)L.capacity * I * 2);
+  L.acc = take((size_t)T * H * 4);
+  L.total = off;
+  return L;
+}
+
+template <typename Tp>
+Tp* at(void* base, size_t off) {
+  return reinterpret_cast<Tp*>(static_cast<char*>(base) + off);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mm_status_string(int status) {
+  switch (status) {
+    case MM_OK: return "MM_OK";
+    case MM_ERR_INVALID_ARG: return "MM_ERR_INVALID_ARG: invalid argument";
+    case MM_ERR_UNSUPPORTED: return "MM_ERR_UNSUPPORTED: shape or device not supported";
+    case MM_ERR_CUDA: return "MM_ERR_CUDA: a CUDA runtime call failed";
+    case MM_ERR_NO_MEMORY: return "MM_ERR_NO_MEMORY: workspace allocation failed or too small";
+    case MM_ERR_DEVICE: return "MM_ERR_DEVICE: a kernel flagged invalid input";
+    case MM_ERR_TIMEOUT: return "MM_ERR_TIMEOUT: a kernel wait timed out";
+    default: return "unknown mm status";
+  }
+}
+
+int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias, int T,
+             int H, int E, int top_k, int renorm, int32_t* topk_ids, float* topk_w,
+             void* stream) {
+  int rc = check_route_shape(T, H, E, top_k);
+  if (rc != MM_OK) return rc;
+  if (!hidden || !router_w || !topk_ids || !topk_w) return MM_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w))
+    return MM_ERR_INVALID_ARG;
+  if (T == 0) return MM_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  if ((rc = device_state(&s)) != MM_OK) return rc;
+  return cuda_status(launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, topk_ids,
+                                  topk_w, nullptr, 0, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t mm_align_capacity(int T, int top_k, int E, int block_m) {
+  if (T < 0 || top_k <= 0 || E <= 0 || block_m <= 0) return -1;
+  return (int64_t)T * top_k + (int64_t)E * (block_m - 1);
+}
+
+int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+             int32_t* sorted_token_ids, int32_t* expert_offsets, int32_t* expert_counts,
+             void* stream) {
+  if (T < 0 || top_k <= 0 || E <= 0 || block_m <= 0) return MM_ERR_INVALID_ARG;
+  if (E > kMaxExperts || top_k > kMaxTopK || block_m > 256) return MM_ERR_UNSUPPORTED;
+  if ((long long)T * top_k + (long long)E * block_m >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
+  if ((T > 0 && !topk_ids) || !sorted_token_ids || !expert_offsets) return MM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  const long long scratch_ints = align_scratch_ints(T, E);
+  if (scratch_ints > 0 && (rc = ensure_ws(s, (size_t)scratch_ints * 4)) != MM_OK) return rc;
+  return cuda_status(launch_align(topk_ids, T, top_k, E, block_m,
+                                  mm_align_capacity(T, top_k, E, block_m), sorted_token_ids,
+                                  expert_offsets, expert_counts, static_cast<int32_t*>(s->ws),
+                                  s->status, static_cast<cudaStream_t>(stream)));
+}
+
+int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
+                    const int32_t* sorted_token_ids, const int32_t* expert_offsets,
+                    const float* topk_w, int T, int top_k, int E, int N, int K, int block_m,
+                    void* stream) {
+  if (mode != MM_GEMM_GATE_UP && mode != MM_GEMM_DOWN) return MM_ERR_INVALID_ARG;
+  if (T < 0 || top_k <= 0 || E <= 0 || N <= 0 || K <= 0 || block_m <= 0) return MM_ERR_INVALID_ARG;
+  if (E > kMaxExperts || top_k > kMaxTopK || block_m > 256 || N % 64 != 0 || K % 64 != 0)
+    return MM_ERR_UNSUPPORTED;
+  if (!A || !B || !C || !sorted_token_ids || !expert_offsets) return MM_ERR_INVALID_ARG;
+  if (mode == MM_GEMM_DOWN && !topk_w) return MM_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MM_ERR_INVALID_ARG;
+  const long long capacity = mm_align_capacity(T, top_k, E, block_m);
+  if (capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint16_t* X = static_cast<const uint16_t*>(A);
+  if (mode == MM_GEMM_GATE_UP) {
+    if ((rc = ensure_ws(s, (size_t)capacity * K * 2)) != MM_OK) return rc;
+    uint16_t* xs = static_cast<uint16_t*>(s->ws);
+    if (launch_gather_rows(X, sorted_token_ids, expert_offsets, E, T, top_k, K, capacity, xs,
+                           s->sms, st) != cudaSuccess)
+      return MM_ERR_CUDA;
+    X = xs;
+  }
+  return cuda_status(launch_grouped_gemm(mode, X, B, C, sorted_token_ids, expert_offsets, topk_w,
+                                         T, top_k, E, N, K, capacity, s->sms, s->status, st));
+}
+
+int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
+  if (check_route_shape(T, H, E, top_k) != MM_OK || I <= 0 || I % 64 != 0) return -1;
+  return (int64_t)forward_layout(T, H, E, I, top_k).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The launch sequence of the layer. If `ev` is non-null, events ev[0..6] are
+// recorded on the stream around the stages: route | align | gather | gate_up
+// | down | finalize.
+int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
+                 const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
+                 int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
+                 cudaStream_t st, cudaEvent_t const* ev) {
+  int rc = check_route_shape(T, H, E, top_k);
+  if (rc != MM_OK) return rc;
+  if (I <= 0) return MM_ERR_INVALID_ARG;
+  if (I % 64 != 0) return MM_ERR_UNSUPPORTED;
+  if (!hidden || !router_w || !w_gate_up || !w_down || !out) return MM_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(w_gate_up) ||
+      !aligned16(w_down) || !aligned16(out))
+    return MM_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(T, H, E, I, top_k);
+  if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
+  if (workspace != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MM_ERR_INVALID_ARG;
+    if (workspace_bytes < L.total) return MM_ERR_NO_MEMORY;
+  }
+  if (T == 0) return MM_OK;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  if ((rc = device_state(&s)) != MM_OK) return rc;
+  void* ws = workspace;
+  if (ws == nullptr) {
+    if ((rc = ensure_ws(s, L.total)) != MM_OK) return rc;
+    ws = s->ws;
+  }
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* scratch = at<int32_t>(ws, L.scratch);
+  uint16_t* xs = at<uint16_t>(ws, L.xs);
+  uint16_t* act = at<uint16_t>(ws, L.act);
+  float* acc = at<float>(ws, L.acc);
+  const long long nacc = (long long)T * H;
+  auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
+
+  if (!mark(0)) return MM_ERR_CUDA;
+  if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, st) !=
+          cudaSuccess || !mark(1))
+    return MM_ERR_CUDA;
+  if (launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts, scratch,
+                   s->status, st) != cudaSuccess || !mark(2))
+    return MM_ERR_CUDA;
+  if (launch_gather_rows(hidden, sorted, offsets, E, T, top_k, H, L.capacity, xs, s->sms, st) !=
+          cudaSuccess || !mark(3))
+    return MM_ERR_CUDA;
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, xs, w_gate_up, act, sorted, offsets, nullptr, T, top_k,
+                          E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(4))
+    return MM_ERR_CUDA;
+  if (launch_grouped_gemm(MM_GEMM_DOWN, act, w_down, acc, sorted, offsets, w, T, top_k, E, H, I,
+                          L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(5))
+    return MM_ERR_CUDA;
+  if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(6)) return MM_ERR_CUDA;
+  return MM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
+                      const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E,
+                      int I, int top_k, int renorm, uint16_t* out, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  return forward_impl(hidden, router_w, router_bias, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                      out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,
+                            const float* router_bias, const uint16_t* w_gate_up,
+                            const uint16_t* w_down, int T, int H, int E, int I, int top_k,
+                            int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
+                            void* stream, void* const* events) {
+  if (events == nullptr) return MM_ERR_INVALID_ARG;
+  for (int i = 0; i < MM_PROFILE_EVENTS; ++i)
+    if (events[i] == nullptr) return MM_ERR_INVALID_ARG;
+  return forward_impl(hidden, router_w, router_bias, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                      out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                      reinterpret_cast<cudaEvent_t const*>(events));
+}
+
+int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w, const uint16_t* w_gate_up,
+                   const uint16_t* w_down, int T, int H, int E, int I, int top_k, int renorm,
+                   uint16_t* out, void* stream) {
+  return mm_moe_forward_ex(hidden, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                           out, nullptr, 0, stream);
+}
+
+int mm_poll_device_status(void* stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MM_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, s->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(s->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MM_ERR_CUDA;
+  }
+  if (v & kDevErrTimeout) return MM_ERR_TIMEOUT;
+  if (v & kDevErrBadIds) return MM_ERR_DEVICE;
+  return MM_OK;
+}
+
+void mm_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int cur = 0;
+  const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_dev[d].ws == nullptr) continue;
+    if (cudaSetDevice(d) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      cudaFree(g_dev[d].ws);
+    }
+    g_dev[d].ws = nullptr;
+    g_dev[d].ws_bytes = 0;
+  }
+  if (have_cur) cudaSetDevice(cur);
+}
+
+}  // extern "C"

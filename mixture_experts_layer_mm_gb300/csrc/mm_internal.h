@@ -1,0 +1,58 @@
+// Host-side launchers of the MoE layer's kernels (internal; the public C ABI
+// is include/mm.h and is implemented in api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mm {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+// Token rows per expert segment are padded to this multiple by the forward
+// path; it is also the granularity of the tensor-core N dimension.
+constexpr int kForwardBlockM = 16;
+// Tokens handled by one block of the align kernels.
+constexpr int kAlignBlockTokens = 1024;
+constexpr int kMaxDevices = 64;
+
+// Index of the current CUDA device (0 if the query fails).
+inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) d = 0;
+  return d;
+}
+
+// Router logits + softmax + top-k (+ renorm). If zero_buf is non-null the same
+// launch also zeroes zero_count floats there (zero_count % 4 == 0).
+cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                         int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
+                         float* topk_w, float* zero_buf, long long zero_count, cudaStream_t st);
+
+// Scratch ints the align launch needs (0 when one block covers all tokens).
+long long align_scratch_ints(int T, int E);
+
+cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                         long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
+                         int32_t* scratch, unsigned* err, cudaStream_t st);
+
+// x_sorted[r] = hidden[sorted[r] / top_k] for r < offsets[E] (zeros for padding).
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
+                               const int32_t* offsets, int E, int T, int top_k, int H,
+                               long long capacity, uint16_t* x_sorted, int num_sms,
+                               cudaStream_t st);
+
+// Grouped GEMM on tcgen05. X = token rows [capacity, K] (already in segment
+// order), W = expert weights. mode 0: C = act bf16 [capacity, N] with
+// silu(gate)*up; mode 1: C = fp32 acc [T, N] += topk_w * (X W^T).
+cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, const uint16_t* W, void* C,
+                                const int32_t* sorted, const int32_t* offsets,
+                                const float* topk_w, int T, int top_k, int E, int N, int K,
+                                long long capacity, int num_sms, unsigned* err, cudaStream_t st);
+
+// out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
+cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
+                            cudaStream_t st);
+
+}  // namespace mm

@@ -4,9 +4,12 @@ This module is shared by the CUDA path's tests/benchmark and by the CPU oracle's
 tests. It holds input generation only: no step of the MoE computation lives here.
 
 Recipe (all configs):
-  * ``numpy.random.default_rng(seed)`` (PCG64), float32 standard normals, drawn
-    in this order: hidden, router_w, w_gate_up, w_down, then (skewed sweep
-    only) the expert-rank permutation of the Zipf logit bias.
+  * numpy PCG64 streams, float32 standard normals. Three independent streams
+    per seed: ``default_rng((seed, 0))`` draws hidden; ``default_rng((seed,
+    1))`` draws router_w, w_gate_up, w_down in that order; ``default_rng((seed,
+    2))`` draws the expert-rank permutation of the Zipf logit bias (skewed
+    sweep only). The weights therefore do not depend on T: the decode,
+    prefill and sweep workloads of one model shape share one layer.
   * Each tensor is scaled by its standard deviation in float32 and rounded
     once to bf16 (round to nearest, ties to even); both sides then read the
     same bf16 bit patterns, carried as ``uint16`` arrays.
@@ -91,26 +94,41 @@ def make_inputs(shape: MoEShape, weights: bool = True) -> dict:
     """Draw the inputs of one MoE layer call. Returns a dict of numpy arrays:
     hidden[T,H], router_w[E,H], w_gate_up[E,2I,H], w_down[E,H,I] (uint16 bf16
     bits) and router_bias[E] (float32, or None)."""
-    rng = np.random.default_rng(shape.seed)
-    T, H, E, I = shape.T, shape.H, shape.E, shape.I
+    d = {"hidden": make_hidden(shape)}
+    d.update(make_weights(shape, experts=weights))
+    d["router_bias"] = make_router_bias(shape)
+    return d
+
+
+def make_hidden(shape: MoEShape) -> np.ndarray:
+    rng = np.random.default_rng((shape.seed, 0))
+    return _normal_bf16(rng, (shape.T, shape.H), shape.x_std)
+
+
+def make_weights(shape: MoEShape, experts: bool = True) -> dict:
+    """router_w [E,H] and (if experts) w_gate_up [E,2I,H], w_down [E,H,I]."""
+    rng = np.random.default_rng((shape.seed, 1))
+    H, E, I = shape.H, shape.E, shape.I
     rstd = shape.router_std if shape.router_std is not None else shape.w_std
-    d = {"hidden": _normal_bf16(rng, (T, H), shape.x_std),
-         "router_w": _normal_bf16(rng, (E, H), rstd)}
-    if weights:
+    d = {"router_w": _normal_bf16(rng, (E, H), rstd)}
+    if experts:
         d["w_gate_up"] = _normal_bf16(rng, (E, 2 * I, H), shape.w_std)
         d["w_down"] = _normal_bf16(rng, (E, H, I), shape.w_std)
-    d["router_bias"] = None
-    if shape.zipf_s is not None:
-        perm = rng.permutation(E)
-        d["router_bias"] = zipf_logit_bias(E, shape.zipf_s, perm)
     return d
+
+
+def make_router_bias(shape: MoEShape):
+    if shape.zipf_s is None:
+        return None
+    perm = np.random.default_rng((shape.seed, 2)).permutation(shape.E)
+    return zipf_logit_bias(shape.E, shape.zipf_s, perm)
 
 
 def random_small_inputs(seed: int, T: int, H: int, E: int, I: int,
                         x_std: float = 1.0, w_std: float = 0.1,
                         bias: bool = False) -> dict:
     """Small random cases for property tests (same recipe, free shapes)."""
-    rng = np.random.default_rng(seed)
+    rng = np.random.default_rng((seed, 3))
     d = {"hidden": _normal_bf16(rng, (T, H), x_std),
          "router_w": _normal_bf16(rng, (E, H), w_std),
          "w_gate_up": _normal_bf16(rng, (E, 2 * I, H), w_std),

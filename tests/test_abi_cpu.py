@@ -1,0 +1,96 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every entry point include/mm.h declares, and its host-side argument checks
+return their codes before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_mm_gb300 as mm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib(mmlib):
+    return mm.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "mm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mm_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree(lib):
+    decl = _declared()
+    assert decl == sorted(mm.SIGNATURES), (decl, sorted(mm.SIGNATURES))
+
+
+def test_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(mm.LIB_PATH)
+    for name in _declared():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert mm.status_string(code).startswith("MM_")
+    assert mm.status_string(99) == "unknown mm status"
+
+
+def test_align_capacity(lib):
+    assert mm.mm_align_capacity(64, 8, 128, 16) == 64 * 8 + 128 * 15
+    assert mm.mm_align_capacity(0, 2, 8, 1) == 0
+    assert mm.mm_align_capacity(-1, 2, 8, 16) == -1
+    assert mm.mm_align_capacity(4, 0, 8, 16) == -1
+
+
+def test_workspace_size(lib):
+    n = mm.mm_moe_workspace_size(4096, 2048, 128, 768, 8)
+    cap = 4096 * 8 + 128 * 15
+    assert n >= cap * 2048 * 2 + cap * 768 * 2 + 4096 * 2048 * 4
+    assert mm.mm_moe_workspace_size(4, 100, 8, 64, 2) == -1   # H % 64
+    assert mm.mm_moe_workspace_size(4, 128, 8, 96, 2) == -1   # I % 64
+    assert mm.mm_moe_workspace_size(4, 128, 300, 64, 2) == -1  # E > 256
+
+
+def test_host_checks_before_any_cuda_call(lib):
+    L = mm.lib()
+    # null pointers
+    assert L.mm_route(None, None, None, 4, 64, 8, 2, 1, None, None, None) == mm.MM_ERR_INVALID_ARG
+    # k > E, H % 64, E > 256, k > 32
+    assert L.mm_route(None, None, None, 4, 64, 8, 9, 1, None, None, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_route(None, None, None, 4, 48, 8, 2, 1, None, None, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_route(None, None, None, 4, 64, 300, 2, 1, None, None, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_route(None, None, None, 4, 64, 64, 33, 1, None, None, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_route(None, None, None, -1, 64, 8, 2, 1, None, None, None) == mm.MM_ERR_INVALID_ARG
+    # misaligned pointer
+    assert L.mm_route(8, 16, None, 4, 64, 8, 2, 1, 32, 48, None) == mm.MM_ERR_INVALID_ARG
+    # align: bad block_m, null outputs
+    assert L.mm_align(None, 4, 2, 8, 0, None, None, None, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_align(None, 4, 2, 8, 300, 16, 16, None, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_align(None, 4, 2, 8, 16, None, None, None, None) == mm.MM_ERR_INVALID_ARG
+    # gemm: bad mode, N % 64, missing topk_w in down mode
+    assert L.mm_grouped_gemm(7, 16, 16, 16, 16, 16, None, 4, 2, 8, 64, 64, 16, None) == \
+        mm.MM_ERR_INVALID_ARG
+    assert L.mm_grouped_gemm(0, 16, 16, 16, 16, 16, None, 4, 2, 8, 96, 64, 16, None) == \
+        mm.MM_ERR_UNSUPPORTED
+    assert L.mm_grouped_gemm(1, 16, 16, 16, 16, 16, None, 4, 2, 8, 64, 64, 16, None) == \
+        mm.MM_ERR_INVALID_ARG
+    # forward: I % 64, null out, workspace too small or misaligned
+    assert L.mm_moe_forward(16, 16, 16, 16, 4, 64, 8, 96, 2, 1, 16, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_moe_forward(16, 16, 16, 16, 4, 64, 8, 64, 2, 1, None, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_moe_forward_ex(16, 16, None, 16, 16, 4, 64, 8, 64, 2, 1, 16, 256, 1, None) == \
+        mm.MM_ERR_NO_MEMORY
+    assert L.mm_moe_forward_ex(16, 16, None, 16, 16, 4, 64, 8, 64, 2, 1, 16, 16, 1 << 30, None) == \
+        mm.MM_ERR_INVALID_ARG
+
+
+def test_binding_raises_without_library(monkeypatch, tmp_path):
+    import mixture_experts_layer_mm_gb300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        L.lib()

@@ -1,0 +1,166 @@
+"""End-to-end parity of mm_moe_forward against the CPU oracle.
+
+Every workload shape is run at its full size. Where the oracle's expert loop
+is too slow for the whole batch (T*I*H large), it is evaluated on a sample of
+tokens (routing is per token, so a token's output depends only on its own
+row); the routing and grouping are still compared on the whole batch.
+
+The output is compared with the oracle's expert step taken on the GPU's own
+routing (the conditional oracle) and, where no token is a near tie, with the
+unconditional oracle, within max|err| <= 2e-2 max|ref| and mean relative
+error <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_mm_gb300 as mm
+from mixture_experts_layer_mm_gb300.synthetic import (DECODE, LARGE, PREFILL, SWEEP, SWEEP_T,
+                                                      TINY, MoEShape, make_inputs,
+                                                      random_small_inputs)
+from oracle import moe_oracle as O
+from gpu_util import TIE_GAP, assert_out_close, dev_bf16, f32_dev
+
+pytestmark = pytest.mark.gpu
+
+_WEIGHTS = {}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(mmlib):
+    yield mmlib
+    _WEIGHTS.clear()
+
+
+def _inputs(shape: MoEShape):
+    key = (shape.H, shape.E, shape.I, shape.w_std, shape.router_std, shape.seed)
+    d = make_inputs(shape, weights=key not in _WEIGHTS)
+    if key not in _WEIGHTS:
+        _WEIGHTS.clear()  # one model shape at a time keeps host memory bounded
+        _WEIGHTS[key] = {n: d[n] for n in ("router_w", "w_gate_up", "w_down")}
+        _WEIGHTS[key]["dev"] = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    d.update({n: v for n, v in _WEIGHTS[key].items() if n != "dev"})
+    return d, _WEIGHTS[key]["dev"]
+
+
+def _run(d, dev_w, k, renorm):
+    hidden = dev_bf16(d["hidden"])
+    bias = None if d["router_bias"] is None else f32_dev(d["router_bias"])
+    out = mm.mm_moe_forward(hidden, dev_w["router_w"], dev_w["w_gate_up"], dev_w["w_down"], k,
+                            renorm, router_bias=bias)
+    ids, _ = mm.mm_route(hidden, dev_w["router_w"], k, renorm, router_bias=bias)
+    torch.cuda.synchronize()
+    assert mm.mm_poll_device_status() == mm.MM_OK
+    return out.float().cpu().numpy(), ids.cpu().numpy()
+
+
+def _check(d, k, renorm, out_g, ids_g, sample=None):
+    T = d["hidden"].shape[0]
+    ids_r, w_r, logits = O.route(d["hidden"], d["router_w"], k, renorm, d["router_bias"])
+    tie = O.near_tie_tokens(logits, k, TIE_GAP)
+    assert np.array_equal(ids_g[~tie], ids_r[~tie])
+    tok = np.arange(T) if sample is None else sample
+    probs = O.softmax_over_experts(logits[tok])
+    w_c = O.routing_weights(probs, ids_g[tok], renorm)
+    ref = O.experts_loop(d["hidden"][tok], d["w_gate_up"], d["w_down"], ids_g[tok], w_c)
+    assert_out_close(out_g[tok], ref, "out (conditional oracle)")
+    if not tie[tok].any():
+        ref_u = O.experts_loop(d["hidden"][tok], d["w_gate_up"], d["w_down"], ids_r[tok], w_r[tok])
+        assert_out_close(out_g[tok], ref_u, "out (oracle)")
+
+
+def _sample(T, n, seed=0):
+    if T <= n:
+        return None
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, n, replace=False)]))
+
+
+@pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
+def test_forward_workloads(shape):
+    d, w = _inputs(shape)
+    out, ids = _run(d, w, shape.top_k, shape.renorm)
+    _check(d, shape.top_k, shape.renorm, out, ids, _sample(shape.T, 4096))
+
+
+def test_forward_large_sampled():
+    d, w = _inputs(LARGE)
+    out, ids = _run(d, w, LARGE.top_k, LARGE.renorm)
+    _check(d, LARGE.top_k, LARGE.renorm, out, ids, _sample(LARGE.T, 192))
+
+
+@pytest.mark.parametrize("T", SWEEP_T)
+def test_forward_zipf_sweep(T):
+    shape = SWEEP.with_T(T)
+    d, w = _inputs(shape)
+    out, ids = _run(d, w, shape.top_k, shape.renorm)
+    _check(d, shape.top_k, shape.renorm, out, ids, _sample(T, 1024))
+    load = np.bincount(ids.reshape(-1), minlength=shape.E)
+    if T >= 512:  # the bias skews the load: the busiest expert gets far more than the mean
+        assert load.max() >= 3 * load.mean()
+
+
+@pytest.mark.parametrize("T,H,E,k,I,renorm", [
+    (1, 64, 1, 1, 64, True),      # one expert: the dense SwiGLU MLP
+    (37, 128, 6, 1, 128, True),   # k = 1
+    (50, 192, 8, 8, 64, False),   # every expert on every token
+    (129, 256, 40, 5, 192, True), # E not a power of two, partial m-tiles
+    (300, 64, 256, 32, 64, False),
+    (2000, 128, 16, 4, 320, True),
+])
+def test_forward_shapes(T, H, E, k, I, renorm):
+    d = random_small_inputs(T + 3 * E, T, H, E, I, w_std=0.08, bias=(E % 2 == 0))
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    out, ids = _run(d, dw, k, renorm)
+    _check(d, k, renorm, out, ids)
+
+
+def test_forward_closed_forms():
+    T, H, E, k, I = 200, 128, 8, 2, 128
+    d = random_small_inputs(9, T, H, E, I, w_std=0.08)
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    # gate rows zero -> silu(0) = 0 -> out exactly zero
+    wgu = d["w_gate_up"].copy()
+    wgu[:, :I, :] = 0
+    out0 = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dev_bf16(wgu), dw["w_down"],
+                             k, True)
+    assert (out0.float() == 0).all()
+    # forced routing: every token to experts {1, 6} through the bias, renorm
+    bias = np.full(E, -30.0, dtype=np.float32)
+    bias[[1, 6]] = 30.0
+    out_f = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"],
+                              dw["w_down"], k, True, router_bias=f32_dev(bias))
+    ids, w, _ = O.route(d["hidden"], d["router_w"], k, True, bias)
+    assert (ids == np.array([1, 6])).all()
+    ref = O.experts_loop(d["hidden"], d["w_gate_up"], d["w_down"], ids, w)
+    assert_out_close(out_f.float().cpu().numpy(), ref, "forced routing")
+    # repeat calls give the same routing and outputs within rounding of the
+    # atomic accumulation order
+    a = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                          k, True).float()
+    b = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                          k, True).float()
+    assert (a - b).abs().max().item() <= 1e-2 * a.abs().max().item()
+
+
+def test_forward_caller_workspace_and_t0():
+    T, H, E, k, I = 96, 128, 8, 2, 64
+    d = random_small_inputs(4, T, H, E, I, w_std=0.08)
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    nbytes = mm.mm_moe_workspace_size(T, H, E, I, k)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                            k, True, workspace=ws)
+    ref = mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                            k, True)
+    torch.cuda.synchronize()
+    assert (out.float() - ref.float()).abs().max().item() <= 1e-2 * ref.float().abs().max().item()
+    small = torch.empty(nbytes - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mm.MMError) as ei:
+        mm.mm_moe_forward(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                          k, True, workspace=small)
+    assert ei.value.code == mm.MM_ERR_NO_MEMORY
+    empty = torch.zeros((0, H), dtype=torch.bfloat16, device="cuda")
+    out0 = mm.mm_moe_forward(empty, dw["router_w"], dw["w_gate_up"], dw["w_down"], k, True)
+    assert out0.shape == (0, H)
