@@ -214,6 +214,9 @@ def mm_moe_forward_profiled(hidden, router_w, w_gate_up, w_down, top_k: int, ren
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    for e in events:  # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record()
     ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib().mm_moe_forward_profiled(_ptr(hidden, torch.bfloat16, "hidden"),
                                          _ptr(router_w, torch.bfloat16, "router_w"),

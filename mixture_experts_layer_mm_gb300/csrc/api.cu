@@ -134,10 +134,10 @@ int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* rout
              void* stream) {
   int rc = check_route_shape(T, H, E, top_k);
   if (rc != MM_OK) return rc;
+  if (T == 0) return MM_OK;  // nothing to read or write; pointers may be NULL
   if (!hidden || !router_w || !topk_ids || !topk_w) return MM_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w))
     return MM_ERR_INVALID_ARG;
-  if (T == 0) return MM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
@@ -177,12 +177,12 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   if (T < 0 || top_k <= 0 || E <= 0 || N <= 0 || K <= 0 || block_m <= 0) return MM_ERR_INVALID_ARG;
   if (E > kMaxExperts || top_k > kMaxTopK || block_m > 256 || N % 64 != 0 || K % 64 != 0)
     return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;  // nothing to read or write
   if (!A || !B || !C || !sorted_token_ids || !expert_offsets) return MM_ERR_INVALID_ARG;
   if (mode == MM_GEMM_DOWN && !topk_w) return MM_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return MM_ERR_INVALID_ARG;
   const long long capacity = mm_align_capacity(T, top_k, E, block_m);
   if (capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
-  if (T == 0) return MM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   DevState* s = nullptr;
   int rc = device_state(&s);
@@ -221,6 +221,7 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   if (rc != MM_OK) return rc;
   if (I <= 0) return MM_ERR_INVALID_ARG;
   if (I % 64 != 0) return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;  // nothing to read or write; pointers may be NULL
   if (!hidden || !router_w || !w_gate_up || !w_down || !out) return MM_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(w_gate_up) ||
       !aligned16(w_down) || !aligned16(out))
@@ -231,7 +232,6 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MM_ERR_INVALID_ARG;
     if (workspace_bytes < L.total) return MM_ERR_NO_MEMORY;
   }
-  if (T == 0) return MM_OK;
   std::lock_guard<std::mutex> lock(g_mu);
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
