@@ -343,7 +343,7 @@ def main():
     layer_ms = sum(stage_ms.values())
     roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                      "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
-    launches_per_step = 6 if shape.T <= 1024 else 8
+    launches_per_step = 5 if (shape.T <= 1024 and shape.T * k <= 8192) else 7
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

@@ -99,9 +99,9 @@ int64_t mm_align_capacity(int T, int top_k, int E, int block_m);
  * sorted_token_ids [mm_align_capacity()] int32, expert_offsets [E+1] int32,
  * expert_counts [E] int32 or NULL. 1 <= block_m <= 256. Ids outside [0,E) or
  * repeated within a row are dropped and flag MM_ERR_DEVICE in the device
- * status. For T > 1024 the library's internal workspace holds per-block
- * counts, so calls on one device must not overlap; the result is
- * deterministic (bit-identical on every call).
+ * status. For T > 1024 (or T*top_k > 8192) the library's internal
+ * workspace holds per-block counts, so calls on one device must not overlap;
+ * the result is deterministic (bit-identical on every call).
  */
 int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
              int32_t* sorted_token_ids, int32_t* expert_offsets, int32_t* expert_counts,
@@ -127,9 +127,9 @@ int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
  *         for every real slot (f = sorted_token_ids[r] < T*top_k), by atomic
  *         fp32 adds (summation order is not fixed). The caller zeroes acc.
  *
- * capacity = mm_align_capacity(T, top_k, E, block_m). Gate-up mode stages the
- * gathered rows in the library's internal workspace (calls on one device must
- * not overlap). N and K multiples of 64.
+ * capacity = mm_align_capacity(T, top_k, E, block_m). Token rows are
+ * gathered inside the kernel (TMA tile::gather4); no workspace is used.
+ * N and K multiples of 64.
  */
 int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
                     const int32_t* sorted_token_ids, const int32_t* expert_offsets,
@@ -171,12 +171,12 @@ int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w,
  * Stage timing of mm_moe_forward_ex, for profiling. Same arguments, plus
  * `events`: a host array of MM_PROFILE_EVENTS cudaEvent_t handles (created
  * by the caller with timing enabled). events[i] is recorded on `stream`
- * before stage i and events[6] after the last one; the stages are
- * 0 route, 1 align, 2 gather of token rows, 3 gate_up GEMM, 4 down GEMM,
- * 5 fp32 -> bf16 rounding. No stage is skipped or changed; nothing is
+ * before stage i and events[5] after the last one; the stages are
+ * 0 route, 1 align, 2 gate_up GEMM (token rows gathered inside it), 3 down
+ * GEMM, 4 fp32 -> bf16 rounding. No stage is skipped or changed; nothing is
  * synchronised. (Measurement support: the pages describe no counterpart.)
  */
-#define MM_PROFILE_EVENTS 7
+#define MM_PROFILE_EVENTS 6
 int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,
                             const float* router_bias,
                             const uint16_t* w_gate_up, const uint16_t* w_down,

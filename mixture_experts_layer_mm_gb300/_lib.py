@@ -197,18 +197,18 @@ def mm_moe_forward(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool
     return out
 
 
-PROFILE_STAGES = ("route", "align", "gather", "gate_up", "down", "finalize")
+PROFILE_STAGES = ("route", "align", "gate_up", "down", "finalize")
 
 
 def mm_moe_forward_profiled(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool,
                             events, out=None, router_bias=None, workspace=None, stream=None):
-    """mm_moe_forward that records 7 torch.cuda.Event (timing enabled) around
-    its stages (PROFILE_STAGES) on the stream; returns out."""
+    """mm_moe_forward that records len(PROFILE_STAGES)+1 torch.cuda.Event
+    (timing enabled) around its stages on the stream; returns out."""
     T, H = hidden.shape
     E = router_w.shape[0]
     I = w_down.shape[2]
     if len(events) != len(PROFILE_STAGES) + 1:
-        raise ValueError("need 7 events")
+        raise ValueError(f"need {len(PROFILE_STAGES) + 1} events")
     if out is None:
         out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
     ws_ptr, ws_bytes = None, 0

@@ -9,9 +9,12 @@
 // ballot, plus the counts of the earlier warps and earlier blocks. Nothing is
 // ordered by atomics, so the result is deterministic.
 //
-// T <= 1024: one block does histogram, scan and scatter in a single launch.
-// T >  1024: three launches (per-block counts, one-block scan, scatter);
-// no block ever waits on another.
+// Each block first copies its tokens' ids to shared memory (one coalesced
+// pass), then works from there.
+// Small batches (T <= 1024 and T*k <= 8192): one block does histogram, scan
+// and scatter in a single launch. Otherwise: three launches over blocks of
+// 256 tokens (per-block counts, one-block scan, scatter); no block ever waits
+// on another.
 #include "mm_device.cuh"
 #include "mm_internal.h"
 
@@ -20,19 +23,28 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
+// ids_s[i] = ids of the block's tokens, row-major (ntok x k), one coalesced copy.
+__device__ __forceinline__ void stage_ids(const int32_t* __restrict__ ids, int T, int k, int tok0,
+                                          int* ids_s) {
+  const int ntok = min((int)(blockDim.x), T - tok0);
+  const int n = ntok > 0 ? ntok * k : 0;
+  const int32_t* src = ids + (size_t)tok0 * k;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) ids_s[i] = src[i];
+}
+
 // Ballots of the block's tokens: bal_s[w*E + e] = lanes of warp w whose token
 // picked expert e.
-__device__ __forceinline__ void block_ballots(const int32_t* __restrict__ ids, int T, int k, int E,
-                                              int tok0, uint32_t* bal_s, unsigned* err) {
+__device__ __forceinline__ void block_ballots(const int* ids_s, int T, int k, int E, int tok0,
+                                              uint32_t* bal_s, unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = tok0 + warp * 32 + lane;
+  const int tl = warp * 32 + lane, t = tok0 + tl;
   uint32_t bits[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) bits[q] = 0;
   bool bad = false;
   if (t < T) {
     for (int j = 0; j < k; ++j) {
-      const int id = ids[(size_t)t * k + j];
+      const int id = ids_s[tl * k + j];
       if (id < 0 || id >= E) {
         bad = true;
         continue;
@@ -46,7 +58,7 @@ __device__ __forceinline__ void block_ballots(const int32_t* __restrict__ ids, i
         }
     }
   }
-  if (bad) atomicOr(err, kDevErrBadIds);
+  if (bad && err != nullptr) atomicOr(err, kDevErrBadIds);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     if (q * 32 >= E) break;
@@ -102,18 +114,18 @@ __device__ __forceinline__ void warp_scan_padded(const int* tot, int E, int bm, 
 
 // Writes f = t*k + j of every valid, first-occurrence assignment of the
 // block's tokens at base[e] + pre_s + rank-in-warp.
-__device__ __forceinline__ void block_scatter(const int32_t* __restrict__ ids, int T, int k, int E,
-                                              int tok0, const uint32_t* bal_s, const int* pre_s,
+__device__ __forceinline__ void block_scatter(const int* ids_s, int T, int k, int E, int tok0,
+                                              const uint32_t* bal_s, const int* pre_s,
                                               const int* base, int32_t* __restrict__ sorted) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = tok0 + warp * 32 + lane;
+  const int tl = warp * 32 + lane, t = tok0 + tl;
   if (t >= T) return;
   const uint32_t lt = (1u << lane) - 1u;
   for (int j = 0; j < k; ++j) {
-    const int id = ids[(size_t)t * k + j];
+    const int id = ids_s[tl * k + j];
     if (id < 0 || id >= E) continue;
     bool dup = false;
-    for (int jj = 0; jj < j; ++jj) dup |= ids[(size_t)t * k + jj] == id;
+    for (int jj = 0; jj < j; ++jj) dup |= ids_s[tl * k + jj] == id;
     if (dup) continue;
     const int pos = base[id] + pre_s[warp * E + id] + __popc(bal_s[warp * E + id] & lt);
     sorted[pos] = t * k + j;
@@ -128,10 +140,28 @@ __device__ __forceinline__ void fill_padding(const int* off, const int* tot, int
   for (long long p = off[E] + threadIdx.x; p < capacity; p += blockDim.x) sorted[p] = sentinel;
 }
 
-// Shared layout of the block kernels: bal_s [32*E] u32, pre_s [32*E] i32,
-// tot_s [E] i32, off_s [E+1] i32.
-__host__ __device__ constexpr size_t align_smem_bytes(int E) {
-  return (size_t)(2 * 32 * E + E + E + 1) * 4;
+// Shared layout of the block kernels of W warps: bal_s [W*E] u32, pre_s [W*E]
+// i32, tot_s [E] i32, off_s [E+1] i32, ids_s [W*32*k] i32.
+__host__ __device__ constexpr size_t align_smem_bytes(int W, int E, int k) {
+  return (size_t)(2 * W * E + E + E + 1 + W * 32 * k) * 4;
+}
+
+struct AlignSmem {
+  uint32_t* bal;
+  int* pre;
+  int* tot;
+  int* off;
+  int* ids;
+};
+
+__device__ __forceinline__ AlignSmem carve(unsigned char* smem, int W, int E) {
+  AlignSmem a;
+  a.bal = reinterpret_cast<uint32_t*>(smem);
+  a.pre = reinterpret_cast<int*>(a.bal + W * E);
+  a.tot = a.pre + W * E;
+  a.off = a.tot + E;
+  a.ids = a.off + E + 1;
+  return a;
 }
 
 __global__ void __launch_bounds__(1024) align_single_kernel(
@@ -139,37 +169,39 @@ __global__ void __launch_bounds__(1024) align_single_kernel(
     int32_t* __restrict__ sorted, int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
     unsigned* err) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* bal_s = reinterpret_cast<uint32_t*>(smem);
-  int* pre_s = reinterpret_cast<int*>(bal_s + 32 * E);
-  int* tot_s = pre_s + 32 * E;
-  int* off_s = tot_s + E;
   const int nwarps = blockDim.x >> 5;
-  block_ballots(ids, T, k, E, 0, bal_s, err);
+  const AlignSmem S = carve(smem, nwarps, E);
+  stage_ids(ids, T, k, 0, S.ids);
   __syncthreads();
-  warp_prefix(bal_s, nwarps, E, pre_s, tot_s);
+  block_ballots(S.ids, T, k, E, 0, S.bal, err);
   __syncthreads();
-  if (threadIdx.x < 32) warp_scan_padded(tot_s, E, bm, off_s);
+  warp_prefix(S.bal, nwarps, E, S.pre, S.tot);
+  __syncthreads();
+  if (threadIdx.x < 32) warp_scan_padded(S.tot, E, bm, S.off);
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    offsets[e] = off_s[e];
-    if (e < E && counts != nullptr) counts[e] = tot_s[e];
+    offsets[e] = S.off[e];
+    if (e < E && counts != nullptr) counts[e] = S.tot[e];
   }
-  block_scatter(ids, T, k, E, 0, bal_s, pre_s, off_s, sorted);
-  fill_padding(off_s, tot_s, E, capacity, T * k, sorted);
+  block_scatter(S.ids, T, k, E, 0, S.bal, S.pre, S.off, sorted);
+  fill_padding(S.off, S.tot, E, capacity, T * k, sorted);
 }
 
-__global__ void __launch_bounds__(1024) align_count_kernel(const int32_t* __restrict__ ids, int T,
-                                                           int k, int E,
-                                                           int32_t* __restrict__ block_counts,
-                                                           unsigned* err) {
+__global__ void __launch_bounds__(kAlignBlockTokens) align_count_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int32_t* __restrict__ block_counts,
+    unsigned* err) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* bal_s = reinterpret_cast<uint32_t*>(smem);
+  constexpr int W = kAlignBlockTokens / 32;
+  const AlignSmem S = carve(smem, W, E);
   const int tok0 = blockIdx.x * kAlignBlockTokens;
-  block_ballots(ids, T, k, E, tok0, bal_s, err);
+  stage_ids(ids, T, k, tok0, S.ids);
+  __syncthreads();
+  block_ballots(S.ids, T, k, E, tok0, S.bal, err);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
-    for (int w = 0; w < 32; ++w) c += __popc(bal_s[w * E + e]);
+#pragma unroll
+    for (int w = 0; w < W; ++w) c += __popc(S.bal[w * E + e]);
     block_counts[blockIdx.x * E + e] = c;
   }
 }
@@ -205,61 +237,74 @@ __global__ void __launch_bounds__(256) align_scan_kernel(int nblocks, int T, int
   fill_padding(off_s, tot_s, E, capacity, T * k, sorted);
 }
 
-__global__ void __launch_bounds__(1024) align_scatter_kernel(
+__global__ void __launch_bounds__(kAlignBlockTokens) align_scatter_kernel(
     const int32_t* __restrict__ ids, int T, int k, int E, const int32_t* __restrict__ block_base,
     int32_t* __restrict__ sorted, unsigned* err) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t* bal_s = reinterpret_cast<uint32_t*>(smem);
-  int* pre_s = reinterpret_cast<int*>(bal_s + 32 * E);
-  int* tot_s = pre_s + 32 * E;
-  int* base_s = tot_s + E;
+  constexpr int W = kAlignBlockTokens / 32;
+  const AlignSmem S = carve(smem, W, E);
   const int tok0 = blockIdx.x * kAlignBlockTokens;
-  block_ballots(ids, T, k, E, tok0, bal_s, err);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) base_s[e] = block_base[blockIdx.x * E + e];
+  stage_ids(ids, T, k, tok0, S.ids);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) S.off[e] = block_base[blockIdx.x * E + e];
   __syncthreads();
-  warp_prefix(bal_s, 32, E, pre_s, tot_s);
+  // Bad ids were already flagged by the count kernel.
+  block_ballots(S.ids, T, k, E, tok0, S.bal, nullptr);
   __syncthreads();
-  block_scatter(ids, T, k, E, tok0, bal_s, pre_s, base_s, sorted);
+  warp_prefix(S.bal, W, E, S.pre, S.tot);
+  __syncthreads();
+  block_scatter(S.ids, T, k, E, tok0, S.bal, S.pre, S.off, sorted);
 }
 
 }  // namespace
 
-long long align_scratch_ints(int T, int E) {
-  const long long nb = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
-  return nb <= 1 ? 0 : nb * E;
+namespace {
+inline bool align_single_block(int T, int k) {
+  return T <= kAlignSingleMaxTokens && (long long)T * k <= kAlignSingleMaxIds;
+}
+}  // namespace
+
+long long align_scratch_ints(int T, int E, int k) {
+  if (align_single_block(T, k)) return 0;
+  return (long long)((T + kAlignBlockTokens - 1) / kAlignBlockTokens) * E;
 }
 
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, cudaStream_t st) {
-  const size_t smem = align_smem_bytes(E);
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(align_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)align_smem_bytes(kMaxExperts))) != cudaSuccess)
+    const int single = (int)align_smem_bytes(32, kMaxExperts, 8);  // 32 warps, E=256, 8192 ids
+    const int multi = (int)align_smem_bytes(kAlignBlockTokens / 32, kMaxExperts, kMaxTopK);
+    if ((e = cudaFuncSetAttribute(align_single_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, single)) !=
+        cudaSuccess)
       return e;
     if ((e = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)align_smem_bytes(kMaxExperts))) != cudaSuccess)
+                                  multi)) != cudaSuccess)
       return e;
     if ((e = cudaFuncSetAttribute(align_scatter_kernel,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)align_smem_bytes(kMaxExperts))) != cudaSuccess)
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, multi)) !=
+        cudaSuccess)
       return e;
     attr_done[dev] = true;
   }
-  const int nblocks = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
-  if (nblocks <= 1) {
-    const int nwarps = (T + 31) / 32 < 1 ? 1 : (T + 31) / 32;
+  if (align_single_block(T, top_k)) {
+    const int nwarps = T <= 32 ? 1 : (T + 31) / 32;
+    const size_t smem = align_smem_bytes(nwarps, E, top_k);
     align_single_kernel<<<1, nwarps * 32, smem, st>>>(topk_ids, T, top_k, E, block_m, capacity,
                                                       sorted, offsets, counts, err);
     return cudaGetLastError();
   }
-  align_count_kernel<<<nblocks, 1024, smem, st>>>(topk_ids, T, top_k, E, scratch, err);
+  const int nblocks = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
+  const size_t smem = align_smem_bytes(kAlignBlockTokens / 32, E, top_k);
+  align_count_kernel<<<nblocks, kAlignBlockTokens, smem, st>>>(topk_ids, T, top_k, E, scratch,
+                                                               err);
   align_scan_kernel<<<1, 256, 0, st>>>(nblocks, T, top_k, E, block_m, capacity, scratch, sorted,
                                        offsets, counts);
-  align_scatter_kernel<<<nblocks, 1024, smem, st>>>(topk_ids, T, top_k, E, scratch, sorted, err);
+  align_scatter_kernel<<<nblocks, kAlignBlockTokens, smem, st>>>(topk_ids, T, top_k, E, scratch,
+                                                                 sorted, err);
   return cudaGetLastError();
 }
 

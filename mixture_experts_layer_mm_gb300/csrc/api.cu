@@ -81,7 +81,7 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
+  size_t ids, w, sorted, offsets, counts, scratch, act, acc, total;
   long long capacity;
 };
 
@@ -99,8 +99,7 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
   L.sorted = take((size_t)L.capacity * 4);
   L.offsets = take((size_t)(E + 1) * 4);
   L.counts = take((size_t)E * 4);
-  L.scratch = take((size_t)align_scratch_ints(T, E) * 4);
-  L.xs = take((size_t)L.capacity * H * 2);
+  L.scratch = take((size_t)align_scratch_ints(T, E, k) * 4);
   L.act = take((size_t)L.capacity * I * 2);
   L.acc = take((size_t)T * H * 4);
   L.total = off;
@@ -161,7 +160,7 @@ int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
   DevState* s = nullptr;
   int rc = device_state(&s);
   if (rc != MM_OK) return rc;
-  const long long scratch_ints = align_scratch_ints(T, E);
+  const long long scratch_ints = align_scratch_ints(T, E, top_k);
   if (scratch_ints > 0 && (rc = ensure_ws(s, (size_t)scratch_ints * 4)) != MM_OK) return rc;
   return cuda_status(launch_align(topk_ids, T, top_k, E, block_m,
                                   mm_align_capacity(T, top_k, E, block_m), sorted_token_ids,
@@ -188,17 +187,9 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   int rc = device_state(&s);
   if (rc != MM_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const uint16_t* X = static_cast<const uint16_t*>(A);
-  if (mode == MM_GEMM_GATE_UP) {
-    if ((rc = ensure_ws(s, (size_t)capacity * K * 2)) != MM_OK) return rc;
-    uint16_t* xs = static_cast<uint16_t*>(s->ws);
-    if (launch_gather_rows(X, sorted_token_ids, expert_offsets, E, T, top_k, K, capacity, xs,
-                           s->sms, st) != cudaSuccess)
-      return MM_ERR_CUDA;
-    X = xs;
-  }
-  return cuda_status(launch_grouped_gemm(mode, X, B, C, sorted_token_ids, expert_offsets, topk_w,
-                                         T, top_k, E, N, K, capacity, s->sms, s->status, st));
+  return cuda_status(launch_grouped_gemm(mode, static_cast<const uint16_t*>(A), B, C,
+                                         sorted_token_ids, expert_offsets, topk_w, T, top_k, E, N,
+                                         K, capacity, s->sms, s->status, st));
 }
 
 int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
@@ -210,9 +201,9 @@ int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
 
 namespace {
 
-// The launch sequence of the layer. If `ev` is non-null, events ev[0..6] are
-// recorded on the stream around the stages: route | align | gather | gate_up
-// | down | finalize.
+// The launch sequence of the layer. If `ev` is non-null, events ev[0..5] are
+// recorded on the stream around the stages: route | align | gate_up | down |
+// finalize.
 int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
@@ -246,7 +237,6 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* scratch = at<int32_t>(ws, L.scratch);
-  uint16_t* xs = at<uint16_t>(ws, L.xs);
   uint16_t* act = at<uint16_t>(ws, L.act);
   float* acc = at<float>(ws, L.acc);
   const long long nacc = (long long)T * H;
@@ -259,16 +249,14 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   if (launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts, scratch,
                    s->status, st) != cudaSuccess || !mark(2))
     return MM_ERR_CUDA;
-  if (launch_gather_rows(hidden, sorted, offsets, E, T, top_k, H, L.capacity, xs, s->sms, st) !=
-          cudaSuccess || !mark(3))
-    return MM_ERR_CUDA;
-  if (launch_grouped_gemm(MM_GEMM_GATE_UP, xs, w_gate_up, act, sorted, offsets, nullptr, T, top_k,
-                          E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(4))
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, w_gate_up, act, sorted, offsets, nullptr, T,
+                          top_k, E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+      !mark(3))
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, w_down, acc, sorted, offsets, w, T, top_k, E, H, I,
-                          L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(5))
+                          L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(4))
     return MM_ERR_CUDA;
-  if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(6)) return MM_ERR_CUDA;
+  if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(5)) return MM_ERR_CUDA;
   return MM_OK;
 }
 

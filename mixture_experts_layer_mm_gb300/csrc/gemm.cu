@@ -14,6 +14,11 @@
 //   down mode:     D0 = H rows [m*256, +128)    , D1 = H rows [m*256+128, +128)
 // so the gate_up epilogue finds g and u of one (row, token) in the same thread.
 //
+// Token rows: in gate_up mode they are gathered from hidden by TMA
+// tile::gather4 (four rows per instruction, indexed by sorted_token_ids / k),
+// so no permuted copy of the activations is ever written; in down mode they
+// are the contiguous rows of act.
+//
 // Warp roles (192 threads, one CTA per SM, persistent over a static tile
 // stride): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
 // warps 2-5 = epilogue (each reads its 32-lane quarter of tensor memory).
@@ -49,6 +54,7 @@ struct GemmArgs {
   int w_rows;    // weight rows per expert in the 2-D weight view
   int m_step;    // weight rows per m-tile
   int a1_off;    // row offset of the A1 tile relative to A0
+  int w_evict_first;  // weights are read by one token chunk only: stream them past L2
 };
 
 template <int BN, int STAGES>
@@ -171,12 +177,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer ---
-    if (lane == 0) {
-      const uint64_t pol_w = l2_policy_evict_first();
-      const uint64_t pol_x = l2_policy_evict_last();
-      const int nk = a.K / kGK;
-      int s = 0;
-      uint32_t ph = 0;
+    const uint64_t pol_w = a.w_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_x = l2_policy_evict_last();
+    const int nk = a.K / kGK;
+    int s = 0;
+    uint32_t ph = 0;
+    if (MODE == MM_GEMM_GATE_UP) {
+      // Token rows are gathered straight from hidden: lane i loads rows
+      // 4i..4i+3 of the chunk with one tile::gather4 per stage. The rows of the
+      // next tile are fetched one tile ahead so their latency is hidden.
+      int nxt[4];
+      auto fetch_rows = [&](int tl, int (&rows)[4]) {
+        int e, m, row0, nrows;
+        if (tl < total_tiles) decode_tile<BN>(tl, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;
+          const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
+          rows[j] = f < a.Tk ? f / a.top_k : 0;  // padding rows read row 0 (never stored)
+        }
+      };
+      fetch_rows(blockIdx.x, nxt);
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        if (aborted(&abort_s)) break;
+        int rows[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        fetch_rows(tile + gridDim.x, nxt);
+        int e, m, row0, nrows;
+        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        const int wrow0 = e * a.w_rows + m * a.m_step;
+        const int wrow1 = wrow0 + a.a1_off;
+        const int n_g4 = ((nrows + 15) & ~15) / 4;  // rows the MMA reads, 4 per gather
+        const uint32_t bytes = 2 * Cfg::kABytes + n_g4 * 4 * kGK * 2;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            if (lane == 0) signal_abort(&abort_s, a.err);
+            break;
+          }
+          const uint32_t st = smem_base + s * Cfg::kStageBytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, bytes);
+            tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
+            tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
+          }
+          __syncwarp();
+          if (lane < n_g4)
+            tma_gather4(st + 2 * Cfg::kABytes + lane * 4 * kGK * 2, &tmX, fb, kb * kGK, rows[0],
+                        rows[1], rows[2], rows[3], pol_x);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    } else if (lane == 0) {
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         if (aborted(&abort_s)) break;
         int e, m, row0, nrows;
@@ -294,18 +352,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         } else {
+          // Lane j fetches column j's slot id and routing weight once; the
+          // row loop below takes them by shuffle, so no load sits between
+          // the atomic adds.
           const int h0 = m * 2 * kGM + r_in, h1 = h0 + kGM;
+          int f_l = a.Tk;
+          float w_l = 0.f;
+          if (lane < ncol) {
+            f_l = __ldg(a.sorted + row0 + c0 + lane);
+            if (f_l < a.Tk) w_l = __ldg(a.topk_w + f_l);
+          }
+          const int t_l = f_l / a.top_k;
           float* accp = static_cast<float*>(a.C);
+          const bool ok0 = h0 < a.N, ok1 = h1 < a.N;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j < ncol) {
-              const int f = __ldg(a.sorted + row0 + c0 + j);
-              if (f < a.Tk) {
-                const float wt = __ldg(a.topk_w + f);
-                float* dst = accp + (size_t)(f / a.top_k) * a.N;
-                if (h0 < a.N) red_add_f32(dst + h0, wt * __uint_as_float(g[j]));
-                if (h1 < a.N) red_add_f32(dst + h1, wt * __uint_as_float(u[j]));
-              }
+            const int f = __shfl_sync(0xffffffffu, f_l, j);
+            const int t = __shfl_sync(0xffffffffu, t_l, j);
+            const float wt = __shfl_sync(0xffffffffu, w_l, j);
+            if (j < ncol && f < a.Tk) {
+              float* dst = accp + (size_t)t * a.N;
+              if (ok0) red_add_f32(dst + h0, wt * __uint_as_float(g[j]));
+              if (ok1) red_add_f32(dst + h1, wt * __uint_as_float(u[j]));
             }
           }
         }
@@ -384,6 +452,9 @@ cudaError_t launch_cfg(const uint16_t* X, const uint16_t* W, void* C, const int3
   a.K = K;
   a.Tk = T * top_k;
   a.top_k = top_k;
+  // With more than about half a chunk of rows per expert on average, several
+  // token chunks read each weight tile: keep the weights at normal priority.
+  a.w_evict_first = (long long)T * top_k <= (long long)E * (BN / 2) ? 1 : 0;
   if (MODE == MM_GEMM_GATE_UP) {
     a.w_rows = 2 * N;
     a.m_step = kGM;
@@ -397,35 +468,14 @@ cudaError_t launch_cfg(const uint16_t* X, const uint16_t* W, void* C, const int3
   }
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN)) return cudaErrorInvalidValue;
+  // gate_up: X = hidden [T, K], gathered one row per box row; down: X = act [capacity, K].
+  const bool ok_x = MODE == MM_GEMM_GATE_UP ? make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1)
+                                           : make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN);
+  if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
   grouped_gemm_kernel<MODE, BN, STAGES><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
   return cudaGetLastError();
-}
-
-// x_sorted[r] = hidden[sorted[r] / k] (zeros for padding rows), one warp per
-// row, 16-byte loads and stores.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden,
-                                                          const int32_t* __restrict__ sorted,
-                                                          const int32_t* __restrict__ offsets,
-                                                          int E, int Tk, int k, int H,
-                                                          uint16_t* __restrict__ xs) {
-  const int m_pad = offsets[E];
-  const int lane = threadIdx.x & 31;
-  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
-  const int vec = H / 8;
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < m_pad;
-       r += nw) {
-    const int f = sorted[r];
-    uint4* dst = reinterpret_cast<uint4*>(xs + r * H);
-    if (f < Tk) {
-      const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(f / k) * H);
-      for (int c = lane; c < vec; c += 32) dst[c] = __ldg(src + c);
-    } else {
-      for (int c = lane; c < vec; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
 }
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
@@ -451,19 +501,6 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, const uint16_t* W, 
                                                K, capacity, num_sms, err, st);
   return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, W, C, sorted, offsets, topk_w, T, top_k, E, N, K,
                                           capacity, num_sms, err, st);
-}
-
-cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
-                               const int32_t* offsets, int E, int T, int top_k, int H,
-                               long long capacity, uint16_t* x_sorted, int num_sms,
-                               cudaStream_t st) {
-  long long blocks = (capacity + 7) / 8;
-  const long long cap_blocks = (long long)num_sms * 8;
-  if (blocks > cap_blocks) blocks = cap_blocks;
-  if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(hidden, sorted, offsets, E, T * top_k, top_k, H,
-                                                  x_sorted);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

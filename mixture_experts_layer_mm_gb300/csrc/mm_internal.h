@@ -13,8 +13,11 @@ constexpr int kMaxTopK = 32;
 // Token rows per expert segment are padded to this multiple by the forward
 // path; it is also the granularity of the tensor-core N dimension.
 constexpr int kForwardBlockM = 16;
-// Tokens handled by one block of the align kernels.
-constexpr int kAlignBlockTokens = 1024;
+// Align: one block does everything when T <= kAlignSingleMaxTokens and
+// T*k <= kAlignSingleMaxIds; otherwise blocks of kAlignBlockTokens tokens.
+constexpr int kAlignSingleMaxTokens = 1024;
+constexpr int kAlignSingleMaxIds = 8192;
+constexpr int kAlignBlockTokens = 256;
 constexpr int kMaxDevices = 64;
 
 // Index of the current CUDA device (0 if the query fails).
@@ -31,21 +34,16 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          float* topk_w, float* zero_buf, long long zero_count, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
-long long align_scratch_ints(int T, int E);
+long long align_scratch_ints(int T, int E, int top_k);
 
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, cudaStream_t st);
 
-// x_sorted[r] = hidden[sorted[r] / top_k] for r < offsets[E] (zeros for padding).
-cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
-                               const int32_t* offsets, int E, int T, int top_k, int H,
-                               long long capacity, uint16_t* x_sorted, int num_sms,
-                               cudaStream_t st);
-
-// Grouped GEMM on tcgen05. X = token rows [capacity, K] (already in segment
-// order), W = expert weights. mode 0: C = act bf16 [capacity, N] with
-// silu(gate)*up; mode 1: C = fp32 acc [T, N] += topk_w * (X W^T).
+// Grouped GEMM on tcgen05. mode 0: X = hidden [T, K], rows gathered through
+// sorted / top_k, C = act bf16 [capacity, N] with silu(gate)*up; mode 1:
+// X = act [capacity, K] in segment order, C = fp32 acc [T, N] += topk_w *
+// (X W^T). W = expert weights.
 cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, const uint16_t* W, void* C,
                                 const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,

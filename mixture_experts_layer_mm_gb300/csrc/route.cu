@@ -3,11 +3,15 @@
 // order, optional renormalisation ("mini-sglang guide, chapter 7", paragraph
 // on layers/moe.py; "模型与权重加载", ModelConfig: norm_topk_prob).
 //
-// One CTA = 4 warps = 64 tokens x all experts. The logits GEMM is 2*T*E*H
-// flops (under 1 % of the layer), so it runs on warp-level mma.sync with a
-// double-buffered cp.async pipeline; each warp then owns 16 tokens and does
-// the softmax and the k rounds of warp arg-max on the logits held in shared
-// memory. Logits never reach global memory.
+// The logits GEMM is 2*T*E*H flops (under 1 % of the layer) but reads the
+// whole router matrix for every 64-token tile, so one CTA per tile is
+// latency-bound. Here a thread-block cluster of KS CTAs (KS <= 8) shares a
+// tile: CTA r loads and multiplies only the K-slice [r*H/KS, (r+1)*H/KS) with
+// all its chunks in flight at once (warp-level mma.sync, fp32 accumulate),
+// keeps its partial logits in shared memory, and after a cluster barrier
+// each CTA sums the KS partials of 64/KS tokens through distributed shared
+// memory in rank order (so the result does not depend on timing) and runs
+// the softmax and k rounds of warp arg-max. Logits never reach global memory.
 #include <float.h>
 
 #include "mm_device.cuh"
@@ -16,10 +20,32 @@
 namespace mm {
 namespace {
 
-constexpr int kRtTok = 64;        // tokens per CTA
-constexpr int kRtKc = 64;         // K per pipeline stage
+constexpr int kRtTok = 64;        // tokens per cluster tile
+constexpr int kRtKc = 64;         // K per cp.async chunk
 constexpr int kRtLd = kRtKc + 8;  // padded smem row (bf16): 144 B, conflict-free ldmatrix
 constexpr int kRtThreads = 128;
+constexpr int kRtBufs = 4;        // chunks in flight per CTA
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Loads a float from the shared memory of CTA `rank` of this cluster, at the
+// offset `local` has in this CTA.
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;  // 0 source bytes -> the 16 bytes are zero-filled
@@ -55,16 +81,18 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 template <int EP>
 __global__ void __launch_bounds__(kRtThreads) route_kernel(
     const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
-    const float* __restrict__ bias, int T, int H, int E, int top_k, int renorm,
+    const float* __restrict__ bias, int T, int H, int E, int top_k, int renorm, int ks,
     int32_t* __restrict__ ids_out, float* __restrict__ w_out, float* __restrict__ zero_buf,
     long long zero_count) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [2][kRtTok][kRtLd]
-  uint16_t* ws = xs + 2 * kRtTok * kRtLd;             // [2][EP][kRtLd]
-  float* logit_s = reinterpret_cast<float*>(smem);    // after the GEMM: [kRtTok][EP + 1]
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [kRtBufs][kRtTok][kRtLd]
+  uint16_t* ws = xs + kRtBufs * kRtTok * kRtLd;       // [kRtBufs][EP][kRtLd]
+  float* part = reinterpret_cast<float*>(smem);       // after the GEMM: [kRtTok][EP + 1]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * kRtTok;
+  const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
+  const int t0 = (blockIdx.x / ks) * kRtTok;
+  const int hs = H / ks, hbase = (int)rank * hs;
 
   if (zero_buf != nullptr) {  // fused zeroing of the fp32 output accumulator
     float4* z = reinterpret_cast<float4*>(zero_buf);
@@ -74,38 +102,37 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  auto load_stage = [&](int buf, int kc) {
-    for (int i = tid; i < kRtTok * 8; i += kRtThreads) {
-      const int r = i >> 3, c = i & 7, t = t0 + r;
-      const uint32_t dst = smem_u32(xs + (buf * kRtTok + r) * kRtLd + c * 8);
-      const bool ok = t < T;
-      cp_async16(dst, hidden + (ok ? (size_t)t * H + kc + c * 8 : 0), ok);
+  const int nk = hs / kRtKc;
+  auto load_chunk = [&](int c) {
+    if (c < nk) {
+      const int buf = c % kRtBufs, kc = hbase + c * kRtKc;
+      for (int i = tid; i < kRtTok * 8; i += kRtThreads) {
+        const int r = i >> 3, cc = i & 7, t = t0 + r;
+        const uint32_t dst = smem_u32(xs + (buf * kRtTok + r) * kRtLd + cc * 8);
+        const bool ok = t < T;
+        cp_async16(dst, hidden + (ok ? (size_t)t * H + kc + cc * 8 : 0), ok);
+      }
+      for (int i = tid; i < EP * 8; i += kRtThreads) {
+        const int r = i >> 3, cc = i & 7;
+        const uint32_t dst = smem_u32(ws + (buf * EP + r) * kRtLd + cc * 8);
+        const bool ok = r < E;
+        cp_async16(dst, router_w + (ok ? (size_t)r * H + kc + cc * 8 : 0), ok);
+      }
     }
-    for (int i = tid; i < EP * 8; i += kRtThreads) {
-      const int r = i >> 3, c = i & 7;
-      const uint32_t dst = smem_u32(ws + (buf * EP + r) * kRtLd + c * 8);
-      const bool ok = r < E;
-      cp_async16(dst, router_w + (ok ? (size_t)r * H + kc + c * 8 : 0), ok);
-    }
-    cp_async_commit();
+    cp_async_commit();  // empty groups keep the group count uniform
   };
 
   float acc[EP / 8][4];
 #pragma unroll
   for (int j = 0; j < EP / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  const int nk = H / kRtKc;
-  load_stage(0, 0);
-  for (int kc = 0; kc < nk; ++kc) {
-    if (kc + 1 < nk) {
-      load_stage((kc + 1) & 1, (kc + 1) * kRtKc);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+#pragma unroll
+  for (int c = 0; c < kRtBufs; ++c) load_chunk(c);
+  for (int c = 0; c < nk; ++c) {
+    cp_async_wait<kRtBufs - 1>();
     __syncthreads();
-    const uint16_t* xb = xs + (kc & 1) * kRtTok * kRtLd;
-    const uint16_t* wb = ws + (kc & 1) * EP * kRtLd;
+    const uint16_t* xb = xs + (c % kRtBufs) * kRtTok * kRtLd;
+    const uint16_t* wb = ws + (c % kRtBufs) * EP * kRtLd;
 #pragma unroll
     for (int kk = 0; kk < kRtKc / 16; ++kk) {
       uint32_t a0, a1, a2, a3;
@@ -122,31 +149,44 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       }
     }
     __syncthreads();
+    load_chunk(c + kRtBufs);
   }
+  cp_async_wait<0>();
+  __syncthreads();
 
-  // Accumulators -> shared logits [token][expert].
+  // Partial logits of this K-slice -> shared [token][expert].
   {
     const int r0 = warp * 16 + (lane >> 2), c0 = 2 * (lane & 3);
 #pragma unroll
     for (int j = 0; j < EP / 8; ++j) {
-      logit_s[r0 * (EP + 1) + j * 8 + c0] = acc[j][0];
-      logit_s[r0 * (EP + 1) + j * 8 + c0 + 1] = acc[j][1];
-      logit_s[(r0 + 8) * (EP + 1) + j * 8 + c0] = acc[j][2];
-      logit_s[(r0 + 8) * (EP + 1) + j * 8 + c0 + 1] = acc[j][3];
+      part[r0 * (EP + 1) + j * 8 + c0] = acc[j][0];
+      part[r0 * (EP + 1) + j * 8 + c0 + 1] = acc[j][1];
+      part[(r0 + 8) * (EP + 1) + j * 8 + c0] = acc[j][2];
+      part[(r0 + 8) * (EP + 1) + j * 8 + c0 + 1] = acc[j][3];
     }
   }
-  __syncthreads();
+  if (ks > 1)
+    cluster_sync();  // every CTA's partials are visible cluster-wide
+  else
+    __syncthreads();
 
   constexpr int Q = EP / 32;  // logits per lane
-  for (int rr = 0; rr < 16; ++rr) {
-    const int r = warp * 16 + rr, t = t0 + r;
+  const int per = kRtTok / ks;  // tokens this CTA finishes
+  for (int rr = warp; rr < per; rr += kRtThreads / 32) {
+    const int r = (int)rank * per + rr, t = t0 + r;
     if (t >= T) break;
     float l[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q) {
       const int e = lane + 32 * q;
       l[q] = -INFINITY;
-      if (e < E) l[q] = logit_s[r * (EP + 1) + e] + (bias != nullptr ? bias[e] : 0.f);
+      if (e < E) {
+        float v = 0.f;
+        for (int src = 0; src < ks; ++src)  // fixed order: deterministic sum
+          v += ks > 1 ? ld_dsmem_f32(part + r * (EP + 1) + e, (uint32_t)src)
+                      : part[r * (EP + 1) + e];
+        l[q] = v + (bias != nullptr ? bias[e] : 0.f);
+      }
     }
     float m = -INFINITY;
 #pragma unroll
@@ -215,22 +255,46 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       base += __popc(bal);
     }
   }
+  if (ks > 1) cluster_sync();  // keep this CTA's partials alive until every reader is done
 }
 
 template <int EP>
 cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                       int H, int E, int top_k, int renorm, int32_t* ids, float* w, float* zero_buf,
                       long long zero_count, cudaStream_t st) {
-  const size_t gemm_bytes = (size_t)2 * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
-  const size_t logit_bytes = (size_t)kRtTok * (EP + 1) * sizeof(float);
-  const size_t smem = gemm_bytes > logit_bytes ? gemm_bytes : logit_bytes;
-  cudaError_t e = cudaFuncSetAttribute(route_kernel<EP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const int grid = (T + kRtTok - 1) / kRtTok;
-  route_kernel<EP><<<grid, kRtThreads, smem, st>>>(hidden, router_w, bias, T, H, E, top_k, renorm,
-                                                   ids, w, zero_buf, zero_count);
-  return cudaGetLastError();
+  const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
+  const size_t part_bytes = (size_t)kRtTok * (EP + 1) * sizeof(float);
+  const size_t smem = gemm_bytes > part_bytes ? gemm_bytes : part_bytes;
+  static bool attr_done[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel<EP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  // Cluster size: the largest of 8, 4, 2 that splits H into 64-wide chunks.
+  int ks = 1;
+  for (int c = 8; c > 1; c >>= 1)
+    if (H % (kRtKc * c) == 0) {
+      ks = c;
+      break;
+    }
+  const int tiles = (T + kRtTok - 1) / kRtTok;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles * ks, 1, 1);
+  cfg.blockDim = dim3(kRtThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_kernel<EP>, hidden, router_w, bias, T, H, E, top_k, renorm,
+                            ks, ids, w, zero_buf, zero_count);
 }
 
 }  // namespace

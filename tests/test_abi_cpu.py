@@ -50,7 +50,7 @@ def test_align_capacity(lib):
 def test_workspace_size(lib):
     n = mm.mm_moe_workspace_size(4096, 2048, 128, 768, 8)
     cap = 4096 * 8 + 128 * 15
-    assert n >= cap * 2048 * 2 + cap * 768 * 2 + 4096 * 2048 * 4
+    assert n >= cap * 768 * 2 + 4096 * 2048 * 4   # act + fp32 accumulator
     assert mm.mm_moe_workspace_size(4, 100, 8, 64, 2) == -1   # H % 64
     assert mm.mm_moe_workspace_size(4, 128, 8, 96, 2) == -1   # I % 64
     assert mm.mm_moe_workspace_size(4, 128, 300, 64, 2) == -1  # E > 256
