@@ -108,6 +108,32 @@ int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
              void* stream);
 
 /*
+ * mm_align for callers that cannot allocate device memory: a serving engine
+ * whose memory pool already owns the device, or code running where neither a
+ * cudaMalloc nor the device-wide synchronisation that growing mm_align's
+ * internal workspace implies is allowed. (The pages have no counterpart: this
+ * entry point exists for such callers only.)
+ *
+ * Same arguments, outputs and result as mm_align (bit-identical). The caller
+ * still passes every input and output. When mm_align would use scratch memory
+ * (T > 1024 or T*top_k > 8192: ceil(T/256) * E per-block counts), this entry
+ * point keeps those counts in a fixed device array of
+ * MM_ALIGN_NOALLOC_MAX_SCRATCH_INTS int32 (128 KB) that every GPU loading the
+ * library holds until exit; sizes needing more (e.g. T > 65536 at E = 128)
+ * return MM_ERR_UNSUPPORTED before any CUDA call. The first call on a device
+ * looks up the array's device address (a one-time set-up, no allocation);
+ * make that first call before any stream capture. Every call shares the one
+ * array per device, so calls whose executions overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller. Each
+ * call rewrites every entry it reads, so nothing has to be cleared between
+ * calls.
+ */
+#define MM_ALIGN_NOALLOC_MAX_SCRATCH_INTS 32768
+int mm_align_noalloc(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
+                     int32_t* sorted_token_ids, int32_t* expert_offsets, int32_t* expert_counts,
+                     void* stream);
+
+/*
  * One grouped GEMM over the expert segments that mm_align produced, on the
  * 5th-generation tensor cores (bf16 operands, fp32 accumulation in tensor
  * memory). For every expert e and every slot r in its segment:

@@ -33,6 +33,7 @@ SIGNATURES = {
     "mm_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mm_align_capacity": (_I64, [_I, _I, _I, _I]),
     "mm_align": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "mm_align_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "mm_grouped_gemm": (_I, [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "mm_moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "mm_moe_workspace_size": (_I64, [_I, _I, _I, _I, _I]),
@@ -144,6 +145,18 @@ def mm_align(topk_ids, E: int, block_m: int, sorted_token_ids=None, expert_offse
                           _ptr(expert_offsets, torch.int32, "expert_offsets"),
                           _ptr(expert_counts, torch.int32, "expert_counts"),
                           _stream(stream)), "mm_align")
+    return sorted_token_ids, expert_offsets, expert_counts
+
+
+def mm_align_noalloc(topk_ids, E: int, block_m: int, sorted_token_ids, expert_offsets,
+                     expert_counts=None, stream=None):
+    """mm_align with caller-owned outputs and no device allocation (see include/mm.h)."""
+    T, k = topk_ids.shape
+    _check(lib().mm_align_noalloc(_ptr(topk_ids, torch.int32, "topk_ids"), T, k, E, block_m,
+                                  _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                                  _ptr(expert_offsets, torch.int32, "expert_offsets"),
+                                  _ptr(expert_counts, torch.int32, "expert_counts"),
+                                  _stream(stream)), "mm_align_noalloc")
     return sorted_token_ids, expert_offsets, expert_counts
 
 

@@ -113,6 +113,18 @@ Tp* at(void* base, size_t off) {
 
 }  // namespace
 
+namespace mm {
+
+int current_status_word(unsigned** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  const int rc = device_state(&s);
+  if (rc == MM_OK) *out = s->status;
+  return rc;
+}
+
+}  // namespace mm
+
 extern "C" {
 
 const char* mm_status_string(int status) {

@@ -27,6 +27,10 @@ inline int current_device() {
   return d;
 }
 
+// Device address of the current device's status word (see
+// mm_poll_device_status); sets up the device state on first use.
+int current_status_word(unsigned** out);
+
 // Router logits + softmax + top-k (+ renorm). If zero_buf is non-null the same
 // launch also zeroes zero_count floats there (zero_count % 4 == 0).
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
