@@ -343,7 +343,11 @@ def main():
     layer_ms = sum(stage_ms.values())
     roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                      "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
-    launches_per_step = 5 if (shape.T <= 1024 and shape.T * k <= 8192) else 7
+    fused_align = shape.T <= 64 and shape.T * k <= 8192
+    single_align = shape.T <= 1024 and shape.T * k <= 8192
+    gathers_in_gemm = shape.T * k <= 64 * shape.E
+    launches_per_step = (4 + (0 if fused_align else 1 if single_align else 3)
+                         + (0 if gathers_in_gemm else 1))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

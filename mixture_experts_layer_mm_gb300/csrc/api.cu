@@ -81,7 +81,8 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t ids, w, sorted, offsets, counts, scratch, act, acc, total;
+  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
+  bool gather;  // gate_up gathers token rows itself (no xs region)
   long long capacity;
 };
 
@@ -100,6 +101,8 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.counts = take((size_t)E * 4);
   L.scratch = take((size_t)align_scratch_ints(T, E, k) * 4);
+  L.gather = gate_up_gathers_rows(T, k, E);
+  L.xs = take(L.gather ? 0 : (size_t)L.capacity * H * 2);
   L.act = take((size_t)L.capacity * I * 2);
   L.acc = take((size_t)T * H * 4);
   L.total = off;
@@ -153,7 +156,7 @@ int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* rout
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
   return cuda_status(launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, topk_ids,
-                                  topk_w, nullptr, 0, static_cast<cudaStream_t>(stream)));
+                                  topk_w, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream)));
 }
 
 int64_t mm_align_capacity(int T, int top_k, int E, int block_m) {
@@ -199,9 +202,21 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   int rc = device_state(&s);
   if (rc != MM_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return cuda_status(launch_grouped_gemm(mode, static_cast<const uint16_t*>(A), B, C,
-                                         sorted_token_ids, expert_offsets, topk_w, T, top_k, E, N,
-                                         K, capacity, s->sms, s->status, st));
+  const uint16_t* X = static_cast<const uint16_t*>(A);
+  bool x_is_hidden = mode == MM_GEMM_GATE_UP;
+  if (mode == MM_GEMM_GATE_UP && !gate_up_gathers_rows(T, top_k, E)) {
+    // Many rows per expert: stage the token rows in segment order first.
+    if ((rc = ensure_ws(s, (size_t)capacity * K * 2)) != MM_OK) return rc;
+    uint16_t* xs = static_cast<uint16_t*>(s->ws);
+    if (launch_gather_rows(X, sorted_token_ids, expert_offsets, E, T, top_k, K, capacity, xs,
+                           s->sms, st) != cudaSuccess)
+      return MM_ERR_CUDA;
+    X = xs;
+    x_is_hidden = false;
+  }
+  return cuda_status(launch_grouped_gemm(mode, X, x_is_hidden, B, C, sorted_token_ids,
+                                         expert_offsets, topk_w, T, top_k, E, N, K, capacity,
+                                         s->sms, s->status, st));
 }
 
 int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
@@ -214,8 +229,9 @@ int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
 namespace {
 
 // The launch sequence of the layer. If `ev` is non-null, events ev[0..5] are
-// recorded on the stream around the stages: route | align | gate_up | down |
-// finalize.
+// recorded on the stream around the stages: route (which also groups the
+// tokens when T <= 64) | align (empty then) | gate_up (with the copy of token
+// rows into segment order when that path is taken) | down | finalize.
 int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
@@ -255,18 +271,32 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
 
   if (!mark(0)) return MM_ERR_CUDA;
-  if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, st) !=
-          cudaSuccess || !mark(1))
+  const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
+  const bool fused = route_fuses_align(T, top_k);
+  if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, &fa,
+                   st) != cudaSuccess ||
+      !mark(1))
     return MM_ERR_CUDA;
-  if (launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts, scratch,
-                   s->status, st) != cudaSuccess || !mark(2))
+  if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
+                             scratch, s->status, st) != cudaSuccess)
     return MM_ERR_CUDA;
-  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, w_gate_up, act, sorted, offsets, nullptr, T,
-                          top_k, E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+  if (!mark(2)) return MM_ERR_CUDA;
+  const uint16_t* rows = hidden;
+  if (!L.gather) {
+    uint16_t* xs = at<uint16_t>(ws, L.xs);
+    if (launch_gather_rows(hidden, sorted, offsets, E, T, top_k, H, L.capacity, xs, s->sms, st) !=
+        cudaSuccess)
+      return MM_ERR_CUDA;
+    rows = xs;
+  }
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, rows, L.gather, w_gate_up, act, sorted, offsets,
+                          nullptr, T, top_k, E, I, H, L.capacity, s->sms, s->status, st) !=
+          cudaSuccess ||
       !mark(3))
     return MM_ERR_CUDA;
-  if (launch_grouped_gemm(MM_GEMM_DOWN, act, w_down, acc, sorted, offsets, w, T, top_k, E, H, I,
-                          L.capacity, s->sms, s->status, st) != cudaSuccess || !mark(4))
+  if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, top_k, E,
+                          H, I, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+      !mark(4))
     return MM_ERR_CUDA;
   if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(5)) return MM_ERR_CUDA;
   return MM_OK;

@@ -14,10 +14,13 @@
 //   down mode:     D0 = H rows [m*256, +128)    , D1 = H rows [m*256+128, +128)
 // so the gate_up epilogue finds g and u of one (row, token) in the same thread.
 //
-// Token rows: in gate_up mode they are gathered from hidden by TMA
-// tile::gather4 (four rows per instruction, indexed by sorted_token_ids / k),
-// so no permuted copy of the activations is ever written; in down mode they
-// are the contiguous rows of act.
+// Token rows: in gate_up mode with few rows per expert (decode-sized
+// batches) they are gathered from hidden by TMA tile::gather4 (four rows per
+// instruction, indexed by sorted_token_ids / k), so no permuted copy of the
+// activations is written. With many rows per expert the TMA engine would
+// spend a gather per four rows of every stage, so the rows are first copied
+// into segment order (gather_rows_kernel) and loaded as plain 2-D boxes, like
+// the contiguous act rows of the down mode.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over a static tile
 // stride): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
@@ -55,6 +58,7 @@ struct GemmArgs {
   int m_step;    // weight rows per m-tile
   int a1_off;    // row offset of the A1 tile relative to A0
   int w_evict_first;  // weights are read by one token chunk only: stream them past L2
+  int gather_rows;    // gate_up: token rows come straight from hidden by tile::gather4
 };
 
 template <int BN, int STAGES>
@@ -63,7 +67,8 @@ struct GemmCfg {
   static constexpr int kBBytes = BN * kGK * 2;
   static constexpr int kStageBytes = 2 * kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 4 * BN;  // 2 buffers x (D0, D1) x BN columns
-  static constexpr int kSmemBytes = STAGES * kStageBytes + 1024;
+  static constexpr int kEpiBytes = 4 * 32 * 33 * 4;  // per epilogue warp: 32x33 fp32 tile
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kEpiBytes + 1024;
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
   static_assert(BN % 32 == 0 && BN <= 256, "BN");
@@ -144,6 +149,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t smem_base = (raw_addr + 1023u) & ~1023u;
+  float* epi_tile = reinterpret_cast<float*>(smem_raw + (smem_base - raw_addr) +
+                                             STAGES * Cfg::kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nk = a.K / kGK;
     int s = 0;
     uint32_t ph = 0;
-    if (MODE == MM_GEMM_GATE_UP) {
+    if (MODE == MM_GEMM_GATE_UP && a.gather_rows) {
       // Token rows are gathered straight from hidden: lane i loads rows
       // 4i..4i+3 of the chunk with one tile::gather4 per stage. The rows of the
       // next tile are fetched one tile ahead so their latency is hidden.
@@ -326,6 +333,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
       const int b = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
+      // Down mode: lane j holds the slot id and routing weight of columns
+      // j, j+32, ... of this tile. They are loaded before the wait below, so
+      // their latency hides behind the tile's main loop.
+      int f_t[BN / 32];
+      float w_t[BN / 32];
+      if (MODE == MM_GEMM_DOWN) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          const int c = cc * 32 + lane;
+          f_t[cc] = c < nrows ? __ldg(a.sorted + row0 + c) : a.Tk;
+        }
+#pragma unroll
+        for (int cc = 0; cc < BN / 32; ++cc)
+          w_t[cc] = f_t[cc] < a.Tk ? __ldg(a.topk_w + f_t[cc]) : 0.f;
+      }
       if (!mbar_wait(smem_u32(&tfull[b]), use & 1u)) {
         signal_abort(&abort_s, a.err);
         break;
@@ -333,7 +355,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * 2 * BN);
-      for (int c0 = 0; c0 < nrows; c0 += 32) {
+#pragma unroll
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        const int c0 = cc * 32;
+        if (c0 >= nrows) break;
         uint32_t g[32], u[32];
         tmem_ld_32x32b_x32(tb + c0, g);
         tmem_ld_32x32b_x32(tb + BN + c0, u);
@@ -352,28 +377,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         } else {
-          // Lane j fetches column j's slot id and routing weight once; the
-          // row loop below takes them by shuffle, so no load sits between
-          // the atomic adds.
-          const int h0 = m * 2 * kGM + r_in, h1 = h0 + kGM;
-          int f_l = a.Tk;
-          float w_l = 0.f;
-          if (lane < ncol) {
-            f_l = __ldg(a.sorted + row0 + c0 + lane);
-            if (f_l < a.Tk) w_l = __ldg(a.topk_w + f_l);
-          }
+          // Column j's slot id and routing weight come from lane j by
+          // shuffle. The weighted 32x32 block of each
+          // accumulator goes through this warp's shared tile (row = token) so
+          // that each lane adds 4 consecutive outputs of one token with one
+          // 16-byte vector atomic.
+          const int f_l = f_t[cc];
+          const float w_l = w_t[cc];
           const int t_l = f_l / a.top_k;
           float* accp = static_cast<float*>(a.C);
-          const bool ok0 = h0 < a.N, ok1 = h1 < a.N;
+          const uint64_t pol_acc = l2_policy_evict_last();  // keep the accumulator in L2
+          float* tr = epi_tile + (warp - 2) * 32 * 33;  // [token 32][h 32 + 1 pad]
+          const int hq = m * 2 * kGM + q * 32;            // first h of this warp's rows
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int f = __shfl_sync(0xffffffffu, f_l, j);
-            const int t = __shfl_sync(0xffffffffu, t_l, j);
-            const float wt = __shfl_sync(0xffffffffu, w_l, j);
-            if (j < ncol && f < a.Tk) {
-              float* dst = accp + (size_t)t * a.N;
-              if (ok0) red_add_f32(dst + h0, wt * __uint_as_float(g[j]));
-              if (ok1) red_add_f32(dst + h1, wt * __uint_as_float(u[j]));
+          for (int half = 0; half < 2; ++half) {
+            const int hb = hq + half * kGM;
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float wt = __shfl_sync(0xffffffffu, w_l, j);
+              tr[j * 33 + lane] = wt * __uint_as_float(half == 0 ? g[j] : u[j]);
+            }
+            __syncwarp();
+            const int h4 = (lane & 7) * 4;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int jt = it * 4 + (lane >> 3);
+              const int f = __shfl_sync(0xffffffffu, f_l, jt);
+              const int t = __shfl_sync(0xffffffffu, t_l, jt);
+              if (jt < ncol && f < a.Tk && hb + h4 < a.N) {
+                const float* v = tr + jt * 33 + h4;
+                red_add_v4_f32(accp + (size_t)t * a.N + hb + h4, v[0], v[1], v[2], v[3], pol_acc);
+              }
             }
           }
         }
@@ -428,9 +463,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 }
 
 template <int MODE, int BN, int STAGES>
-cudaError_t launch_cfg(const uint16_t* X, const uint16_t* W, void* C, const int32_t* sorted,
-                       const int32_t* offsets, const float* topk_w, int T, int top_k, int E, int N,
-                       int K, long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
+cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
+                       const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
+                       int top_k, int E, int N, int K, long long capacity, int num_sms,
+                       unsigned* err, cudaStream_t st) {
   using Cfg = GemmCfg<BN, STAGES>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -455,6 +491,7 @@ cudaError_t launch_cfg(const uint16_t* X, const uint16_t* W, void* C, const int3
   // With more than about half a chunk of rows per expert on average, several
   // token chunks read each weight tile: keep the weights at normal priority.
   a.w_evict_first = (long long)T * top_k <= (long long)E * (BN / 2) ? 1 : 0;
+  a.gather_rows = (MODE == MM_GEMM_GATE_UP && x_is_hidden) ? 1 : 0;
   if (MODE == MM_GEMM_GATE_UP) {
     a.w_rows = 2 * N;
     a.m_step = kGM;
@@ -468,14 +505,39 @@ cudaError_t launch_cfg(const uint16_t* X, const uint16_t* W, void* C, const int3
   }
   CUtensorMap tmW, tmX;
   if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM)) return cudaErrorInvalidValue;
-  // gate_up: X = hidden [T, K], gathered one row per box row; down: X = act [capacity, K].
-  const bool ok_x = MODE == MM_GEMM_GATE_UP ? make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1)
-                                           : make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN);
+  // Gathered rows: X = hidden [T, K], one row per box; otherwise X holds the
+  // token rows in segment order [capacity, K].
+  const bool ok_x = a.gather_rows ? make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1)
+                                  : make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN);
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
   grouped_gemm_kernel<MODE, BN, STAGES><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
   return cudaGetLastError();
+}
+
+// x_sorted[r] = hidden[sorted[r] / k] (zeros for padding rows), one warp per
+// row, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden,
+                                                          const int32_t* __restrict__ sorted,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int Tk, int k, int H,
+                                                          uint16_t* __restrict__ xs) {
+  const int m_pad = offsets[E];
+  const int lane = threadIdx.x & 31;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  const int vec = H / 8;
+  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < m_pad;
+       r += nw) {
+    const int f = sorted[r];
+    uint4* dst = reinterpret_cast<uint4*>(xs + r * H);
+    if (f < Tk) {
+      const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(f / k) * H);
+      for (int c = lane; c < vec; c += 32) dst[c] = __ldg(src + c);
+    } else {
+      for (int c = lane; c < vec; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
@@ -492,15 +554,32 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, const uint16_t* W, void* C,
-                                const int32_t* sorted, const int32_t* offsets,
+bool gate_up_gathers_rows(int T, int top_k, int E) {
+  return (long long)T * top_k <= 64LL * E;  // at most ~64 rows per expert on average
+}
+
+cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
+                                void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
   if (mode == MM_GEMM_GATE_UP)
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 4>(X, W, C, sorted, offsets, topk_w, T, top_k, E, N,
-                                               K, capacity, num_sms, err, st);
-  return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, W, C, sorted, offsets, topk_w, T, top_k, E, N, K,
-                                          capacity, num_sms, err, st);
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 4>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
+                                               top_k, E, N, K, capacity, num_sms, err, st);
+  return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
+                                          K, capacity, num_sms, err, st);
+}
+
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
+                               const int32_t* offsets, int E, int T, int top_k, int H,
+                               long long capacity, uint16_t* x_sorted, int num_sms,
+                               cudaStream_t st) {
+  long long blocks = (capacity + 7) / 8;
+  const long long cap_blocks = (long long)num_sms * 8;
+  if (blocks > cap_blocks) blocks = cap_blocks;
+  if (blocks < 1) blocks = 1;
+  gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(hidden, sorted, offsets, E, T * top_k, top_k, H,
+                                                  x_sorted);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

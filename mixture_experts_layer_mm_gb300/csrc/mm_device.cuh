@@ -223,4 +223,12 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v));
 }
 
+// Four consecutive fp32 adds at L2 in one 16-byte vector reduction (addr
+// 16-byte aligned).
+__device__ __forceinline__ void red_add_v4_f32(float* addr, float a, float b, float c, float d,
+                                               uint64_t policy) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "l"(policy));
+}
+
 }  // namespace mm

@@ -31,11 +31,27 @@ inline int current_device() {
 // mm_poll_device_status); sets up the device state on first use.
 int current_status_word(unsigned** out);
 
+// Outputs of the grouping step (see mm_align) when the router runs it itself.
+struct AlignOut {
+  int32_t* sorted;
+  int32_t* offsets;
+  int32_t* counts;
+  int block_m;
+  long long capacity;
+  unsigned* err;
+};
+
+// Whether launch_route can group the tokens by expert in the same launch.
+bool route_fuses_align(int T, int top_k);
+
 // Router logits + softmax + top-k (+ renorm). If zero_buf is non-null the same
-// launch also zeroes zero_count floats there (zero_count % 4 == 0).
+// launch also zeroes zero_count floats there (zero_count % 4 == 0). If
+// fuse_align is non-null and route_fuses_align(T, top_k), the launch also
+// produces the grouping.
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
-                         float* topk_w, float* zero_buf, long long zero_count, cudaStream_t st);
+                         float* topk_w, float* zero_buf, long long zero_count,
+                         const AlignOut* fuse_align, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);
@@ -44,12 +60,22 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, cudaStream_t st);
 
-// Grouped GEMM on tcgen05. mode 0: X = hidden [T, K], rows gathered through
-// sorted / top_k, C = act bf16 [capacity, N] with silu(gate)*up; mode 1:
-// X = act [capacity, K] in segment order, C = fp32 acc [T, N] += topk_w *
-// (X W^T). W = expert weights.
-cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, const uint16_t* W, void* C,
-                                const int32_t* sorted, const int32_t* offsets,
+// Whether the gate_up GEMM should gather token rows from hidden itself
+// (few rows per expert) instead of reading a copy in segment order.
+bool gate_up_gathers_rows(int T, int top_k, int E);
+
+// x_sorted[r] = hidden[sorted[r] / top_k] for r < offsets[E] (zeros for padding).
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
+                               const int32_t* offsets, int E, int T, int top_k, int H,
+                               long long capacity, uint16_t* x_sorted, int num_sms,
+                               cudaStream_t st);
+
+// Grouped GEMM on tcgen05. mode 0: C = act bf16 [capacity, N] = silu(gate) *
+// up; X = hidden [T, K] with rows gathered through sorted / top_k when
+// x_is_hidden, else X = token rows already in segment order [capacity, K].
+// mode 1: X = act [capacity, K], C = fp32 acc [T, N] += topk_w * (X W^T).
+cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
+                                void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st);
 

@@ -12,8 +12,13 @@
 // each CTA sums the KS partials of 64/KS tokens through distributed shared
 // memory in rank order (so the result does not depend on timing) and runs
 // the softmax and k rounds of warp arg-max. Logits never reach global memory.
+//
+// When one cluster covers the whole batch (T <= 64), CTA 0 of the cluster
+// also groups the tokens by expert after the final cluster barrier (which
+// makes every CTA's ids visible to it), saving the separate align launch.
 #include <float.h>
 
+#include "align_block.cuh"
 #include "mm_device.cuh"
 #include "mm_internal.h"
 
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
     const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
     const float* __restrict__ bias, int T, int H, int E, int top_k, int renorm, int ks,
     int32_t* __restrict__ ids_out, float* __restrict__ w_out, float* __restrict__ zero_buf,
-    long long zero_count) {
+    long long zero_count, const AlignOut fa) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [kRtBufs][kRtTok][kRtLd]
   uint16_t* ws = xs + kRtBufs * kRtTok * kRtLd;       // [kRtBufs][EP][kRtLd]
@@ -255,13 +260,21 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       base += __popc(bal);
     }
   }
-  if (ks > 1) cluster_sync();  // keep this CTA's partials alive until every reader is done
+  // Keeps this CTA's partials alive until every reader is done, and publishes
+  // every CTA's ids to the cluster.
+  if (ks > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  if (fa.sorted != nullptr && rank == 0)
+    alignblk::align_one_block(ids_out, T, top_k, E, fa.block_m, fa.capacity, fa.sorted,
+                              fa.offsets, fa.counts, fa.err, smem);
 }
 
 template <int EP>
 cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                       int H, int E, int top_k, int renorm, int32_t* ids, float* w, float* zero_buf,
-                      long long zero_count, cudaStream_t st) {
+                      long long zero_count, const AlignOut& fa, cudaStream_t st) {
   const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
   const size_t part_bytes = (size_t)kRtTok * (EP + 1) * sizeof(float);
   const size_t smem = gemm_bytes > part_bytes ? gemm_bytes : part_bytes;
@@ -294,25 +307,30 @@ cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const fl
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_kernel<EP>, hidden, router_w, bias, T, H, E, top_k, renorm,
-                            ks, ids, w, zero_buf, zero_count);
+                            ks, ids, w, zero_buf, zero_count, fa);
 }
 
 }  // namespace
 
+bool route_fuses_align(int T, int top_k) { return T <= kRtTok && T * top_k <= kAlignSingleMaxIds; }
+
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
-                         float* topk_w, float* zero_buf, long long zero_count, cudaStream_t st) {
+                         float* topk_w, float* zero_buf, long long zero_count,
+                         const AlignOut* fuse_align, cudaStream_t st) {
+  AlignOut fa = {};
+  if (fuse_align != nullptr && route_fuses_align(T, top_k)) fa = *fuse_align;
   if (E <= 32)
     return launch_ep<32>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, st);
+                         zero_buf, zero_count, fa, st);
   if (E <= 64)
     return launch_ep<64>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, st);
+                         zero_buf, zero_count, fa, st);
   if (E <= 128)
     return launch_ep<128>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, st);
+                          zero_buf, zero_count, fa, st);
   return launch_ep<256>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w, zero_buf,
-                        zero_count, st);
+                        zero_count, fa, st);
 }
 
 }  // namespace mm
