@@ -66,55 +66,71 @@ def dist_info():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event (throttle) reasons of one GPU, read through
+    NVML every 10 ms on a background thread while the timed region runs.
+    Read-only queries; nothing about the GPU is changed."""
+    # nvmlClocksEventReasons bits
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
 
     def __init__(self, index: int):
+        import ctypes
+        import threading
         self.index = index
-        self.proc = None
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return
+            self._nvml, self._h, self._ct = lib, h, ctypes
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+                self.max_mhz = float(mx.value)
+        except OSError:
+            self._nvml = None
+
+    def _run(self):
+        ct, lib, h = self._ct, self._nvml, self._h
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and \
+                    get_reasons(h, ct.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            self._stop.wait(0.01)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+        import threading
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
     def summary(self):
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm, mx, reasons = [], 0.0, set()
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml unavailable" if self._nvml is None else "nvml"}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "nvml, 10 ms"}
 
 
 def algorithmic_work(shape, ids: np.ndarray):
@@ -202,7 +218,8 @@ def cpu_baseline(shape, budget_s: float):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 0.6 s of work)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mm", "reference"], default="mm")
     ap.add_argument("--workload", default=synthetic.DECODE.name)
@@ -222,6 +239,8 @@ def main():
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 5  # each step is a full oracle pass over the sample
         run_reference(args, shape, ws, rank)
         if ws > 1:
             import torch.distributed as dist
@@ -268,6 +287,15 @@ def main():
     for _ in range(args.warmup):
         fwd()
     torch.cuda.synchronize()
+    if args.steps is None:  # size the timed region to about 0.6 s so clocks are sampled
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            fwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        args.steps = int(min(5000, max(20, 600.0 / max(e0.elapsed_time(e1) / 5, 1e-3))))
+        args.steps = int(max_over_ranks(float(args.steps)))
     st = mm.mm_poll_device_status()
     if st != mm.MM_OK:
         raise RuntimeError(f"device status after warm-up: {mm.status_string(st)}")
@@ -290,11 +318,12 @@ def main():
     clocks = clk.summary()
 
     # ---- timed region B: same steps, stage events recorded around each kernel
+    nb = min(args.steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mm.PROFILE_STAGES) + 1)]
-           for _ in range(args.steps)]
+           for _ in range(nb)]
     barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(nb):
         mm.mm_moe_forward_profiled(hidden, router_w, w_gu, w_dn, k, renorm, evs[i], out=out,
                                    router_bias=bias)
     torch.cuda.synchronize()
@@ -302,7 +331,7 @@ def main():
     stage_ms = {}
     for j, name in enumerate(mm.PROFILE_STAGES):
         stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
-                                         for i in range(args.steps))
+                                         for i in range(nb))
 
     # ---- timed region C: end to end from pinned host memory through the C ABI
     h_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
@@ -345,9 +374,7 @@ def main():
                      "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
     fused_align = shape.T <= 64 and shape.T * k <= 8192
     single_align = shape.T <= 1024 and shape.T * k <= 8192
-    gathers_in_gemm = shape.T * k <= 64 * shape.E
-    launches_per_step = (4 + (0 if fused_align else 1 if single_align else 3)
-                         + (0 if gathers_in_gemm else 1))
+    launches_per_step = 4 + (0 if fused_align else 1 if single_align else 3)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

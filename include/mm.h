@@ -153,11 +153,9 @@ int mm_align_noalloc(const int32_t* topk_ids, int T, int top_k, int E, int block
  *         for every real slot (f = sorted_token_ids[r] < T*top_k), by atomic
  *         fp32 adds (summation order is not fixed). The caller zeroes acc.
  *
- * capacity = mm_align_capacity(T, top_k, E, block_m). With at most ~64 rows
- * per expert on average the token rows are gathered inside the kernel (TMA
- * tile::gather4); with more, gate_up mode first copies them into segment
- * order in the library's internal workspace (calls on one device must then
- * not overlap). N and K multiples of 64.
+ * capacity = mm_align_capacity(T, top_k, E, block_m). Token rows are
+ * gathered from hidden inside the kernel (TMA tile::gather4 with few rows per
+ * expert, cp.async with many); no workspace is used. N and K multiples of 64.
  */
 int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
                     const int32_t* sorted_token_ids, const int32_t* expert_offsets,
@@ -201,9 +199,7 @@ int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w,
  * by the caller with timing enabled). events[i] is recorded on `stream`
  * before stage i and events[5] after the last one; the stages are
  * 0 route (which also does the grouping when T <= 64), 1 align (then
- * empty), 2 gate_up GEMM (including the copy of token rows into
- * segment order when many rows go to each expert), 3 down GEMM, 4 fp32 ->
- * bf16 rounding. No stage is skipped or changed; nothing is
+ * empty), 2 gate_up GEMM, 3 down GEMM, 4 fp32 -> bf16 rounding. No stage is skipped or changed; nothing is
  * synchronised. (Measurement support: the pages describe no counterpart.)
  */
 #define MM_PROFILE_EVENTS 6

@@ -81,8 +81,7 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
-  bool gather;  // gate_up gathers token rows itself (no xs region)
+  size_t ids, w, sorted, offsets, counts, scratch, act, acc, total;
   long long capacity;
 };
 
@@ -101,8 +100,6 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.counts = take((size_t)E * 4);
   L.scratch = take((size_t)align_scratch_ints(T, E, k) * 4);
-  L.gather = gate_up_gathers_rows(T, k, E);
-  L.xs = take(L.gather ? 0 : (size_t)L.capacity * H * 2);
   L.act = take((size_t)L.capacity * I * 2);
   L.acc = take((size_t)T * H * 4);
   L.total = off;
@@ -202,19 +199,8 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   int rc = device_state(&s);
   if (rc != MM_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const uint16_t* X = static_cast<const uint16_t*>(A);
-  bool x_is_hidden = mode == MM_GEMM_GATE_UP;
-  if (mode == MM_GEMM_GATE_UP && !gate_up_gathers_rows(T, top_k, E)) {
-    // Many rows per expert: stage the token rows in segment order first.
-    if ((rc = ensure_ws(s, (size_t)capacity * K * 2)) != MM_OK) return rc;
-    uint16_t* xs = static_cast<uint16_t*>(s->ws);
-    if (launch_gather_rows(X, sorted_token_ids, expert_offsets, E, T, top_k, K, capacity, xs,
-                           s->sms, st) != cudaSuccess)
-      return MM_ERR_CUDA;
-    X = xs;
-    x_is_hidden = false;
-  }
-  return cuda_status(launch_grouped_gemm(mode, X, x_is_hidden, B, C, sorted_token_ids,
+  return cuda_status(launch_grouped_gemm(mode, static_cast<const uint16_t*>(A),
+                                         mode == MM_GEMM_GATE_UP, B, C, sorted_token_ids,
                                          expert_offsets, topk_w, T, top_k, E, N, K, capacity,
                                          s->sms, s->status, st));
 }
@@ -230,8 +216,7 @@ namespace {
 
 // The launch sequence of the layer. If `ev` is non-null, events ev[0..5] are
 // recorded on the stream around the stages: route (which also groups the
-// tokens when T <= 64) | align (empty then) | gate_up (with the copy of token
-// rows into segment order when that path is taken) | down | finalize.
+// tokens when T <= 64) | align (empty then) | gate_up | down | finalize.
 int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
@@ -281,17 +266,8 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
                              scratch, s->status, st) != cudaSuccess)
     return MM_ERR_CUDA;
   if (!mark(2)) return MM_ERR_CUDA;
-  const uint16_t* rows = hidden;
-  if (!L.gather) {
-    uint16_t* xs = at<uint16_t>(ws, L.xs);
-    if (launch_gather_rows(hidden, sorted, offsets, E, T, top_k, H, L.capacity, xs, s->sms, st) !=
-        cudaSuccess)
-      return MM_ERR_CUDA;
-    rows = xs;
-  }
-  if (launch_grouped_gemm(MM_GEMM_GATE_UP, rows, L.gather, w_gate_up, act, sorted, offsets,
-                          nullptr, T, top_k, E, I, H, L.capacity, s->sms, s->status, st) !=
-          cudaSuccess ||
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, true, w_gate_up, act, sorted, offsets, nullptr,
+                          T, top_k, E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess ||
       !mark(3))
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, top_k, E,

@@ -14,17 +14,19 @@
 //   down mode:     D0 = H rows [m*256, +128)    , D1 = H rows [m*256+128, +128)
 // so the gate_up epilogue finds g and u of one (row, token) in the same thread.
 //
-// Token rows: in gate_up mode with few rows per expert (decode-sized
-// batches) they are gathered from hidden by TMA tile::gather4 (four rows per
-// instruction, indexed by sorted_token_ids / k), so no permuted copy of the
-// activations is written. With many rows per expert the TMA engine would
-// spend a gather per four rows of every stage, so the rows are first copied
-// into segment order (gather_rows_kernel) and loaded as plain 2-D boxes, like
-// the contiguous act rows of the down mode.
+// Token rows (B): the contiguous act rows of the down mode come by 2-D TMA
+// boxes. In gate_up mode they are gathered from hidden through
+// sorted_token_ids / k: with few rows per expert (decode-sized batches) by TMA
+// tile::gather4, four rows per instruction; with many rows per expert by four
+// warps of 16-byte cp.async (the TMA engine would spend one gather per four
+// rows of every stage), straight into the swizzled layout. hidden stays in L2,
+// and no permuted copy of the activations is ever written.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over a static tile
-// stride): warp 0 = TMA producer, warp 1 = TMEM allocator + MMA issuer,
-// warps 2-5 = epilogue (each reads its 32-lane quarter of tensor memory).
+// Warp roles (320 threads, one CTA per SM, persistent over a static tile
+// stride): warp 0 = weight (A) TMA producer with a deep ring, warps 6-9 =
+// token (B) producer (warp 6 alone for TMA), warp 1 = TMEM allocator + MMA
+// issuer, warps 2-5 = epilogue (each reads its 32-lane quarter of tensor
+// memory).
 // Two accumulator buffers let the epilogue of one tile overlap the
 // main loop of the next.
 //
@@ -44,7 +46,7 @@ namespace {
 
 constexpr int kGM = 128;  // weight rows per MMA
 constexpr int kGK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;  // 10 warps: producers 0 and 6-9, MMA 1, epilogue 2-5
 
 struct GemmArgs {
   const int32_t* sorted;   // [capacity]
@@ -58,21 +60,50 @@ struct GemmArgs {
   int m_step;    // weight rows per m-tile
   int a1_off;    // row offset of the A1 tile relative to A0
   int w_evict_first;  // weights are read by one token chunk only: stream them past L2
-  int gather_rows;    // gate_up: token rows come straight from hidden by tile::gather4
+  int b_mode;         // how token rows reach shared memory (kB*)
+  const uint16_t* hidden;  // kBLsuGather: token rows are read from here
 };
 
-template <int BN, int STAGES>
+// Token-row (B) paths.
+constexpr int kBTma = 0;        // 2-D TMA boxes of rows already in segment order
+constexpr int kBTmaGather = 1;  // TMA tile::gather4 from hidden (few rows per expert)
+constexpr int kBLsuGather = 2;  // four warps of cp.async from hidden (many rows per expert)
+
+// Two shared-memory rings: SA stages of weight tiles (A0 + A1, 32 KB) and SB
+// stages of token tiles (BN rows). The weights are the DRAM stream, so their
+// ring is the deep one; the token rows mostly hit L2.
+template <int MODE, int BN, int SA, int SB>
 struct GemmCfg {
-  static constexpr int kABytes = kGM * kGK * 2;
-  static constexpr int kBBytes = BN * kGK * 2;
-  static constexpr int kStageBytes = 2 * kABytes + kBBytes;
+  static constexpr int kABytes = kGM * kGK * 2;        // one 128-row weight tile
+  static constexpr int kAStageBytes = 2 * kABytes;     // A0 + A1
+  static constexpr int kBStageBytes = BN * kGK * 2;
   static constexpr uint32_t kTmemCols = 4 * BN;  // 2 buffers x (D0, D1) x BN columns
-  static constexpr int kEpiBytes = 4 * 32 * 33 * 4;  // per epilogue warp: 32x33 fp32 tile
-  static constexpr int kSmemBytes = STAGES * kStageBytes + kEpiBytes + 1024;
+  static constexpr int kEpiBytes = MODE == MM_GEMM_DOWN ? 4 * 32 * 33 * 4 : 0;  // transpose tiles
+  static constexpr int kBOffset = SA * kAStageBytes;
+  static constexpr int kEpiOffset = kBOffset + SB * kBStageBytes;
+  static constexpr int kSmemBytes = kEpiOffset + kEpiBytes + 1024;
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
   static_assert(BN % 32 == 0 && BN <= 256, "BN");
+  static_assert(kSmemBytes <= 227 * 1024 - 4096, "shared memory");
 };
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 template <int BN>
 __device__ __forceinline__ void decode_tile(int tile, int n_mtiles, int E, const int* cs,
@@ -102,13 +133,13 @@ __device__ __forceinline__ void signal_abort(int* flag, unsigned* err) {
   atomicOr(err, kDevErrTimeout);
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int SA, int SB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs a) {
-  using Cfg = GemmCfg<BN, STAGES>;
+  using Cfg = GemmCfg<MODE, BN, SA, SB>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * STAGES + 5];
+  __shared__ __align__(8) uint64_t bars[2 * SA + 2 * SB + 5];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int off_s[kMaxExperts + 1];
@@ -149,18 +180,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t smem_base = (raw_addr + 1023u) & ~1023u;
-  float* epi_tile = reinterpret_cast<float*>(smem_raw + (smem_base - raw_addr) +
-                                             STAGES * Cfg::kStageBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
+  float* epi_tile =
+      reinterpret_cast<float*>(smem_raw + (smem_base - raw_addr) + Cfg::kEpiOffset);
+  uint64_t* fullA = bars;
+  uint64_t* emptyA = fullA + SA;
+  uint64_t* fullB = emptyA + SA;
+  uint64_t* emptyB = fullB + SB;
+  uint64_t* tfull = emptyB + SB;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
 
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(smem_u32(&fullA[s]), 1);
+      mbar_init(smem_u32(&emptyA[s]), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(smem_u32(&fullB[s]), a.b_mode == kBLsuGather ? 128 : 1);  // one per loader thread
+      mbar_init(smem_u32(&emptyB[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -181,15 +218,99 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_s;
+  const int nk = a.K / kGK;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer ---
-    const uint64_t pol_w = a.w_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+    // --------------------------------------------- weight (A) TMA producer ---
+    if (lane == 0) {
+      const uint64_t pol_w = a.w_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+      int s = 0;
+      uint32_t ph = 0;
+      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        if (aborted(&abort_s)) break;
+        int e, m, row0, nrows;
+        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        const int wrow0 = e * a.w_rows + m * a.m_step;
+        const int wrow1 = wrow0 + a.a1_off;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(smem_u32(&emptyA[s]), ph ^ 1u)) {
+            signal_abort(&abort_s, a.err);
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_base + s * Cfg::kAStageBytes;
+          const uint32_t fb = smem_u32(&fullA[s]);
+          mbar_arrive_expect_tx(fb, Cfg::kAStageBytes);
+          tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
+          tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
+          if (++s == SA) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp >= 6) {
+    // -------------------------------------------------- token (B) producer ---
     const uint64_t pol_x = l2_policy_evict_last();
-    const int nk = a.K / kGK;
     int s = 0;
     uint32_t ph = 0;
-    if (MODE == MM_GEMM_GATE_UP && a.gather_rows) {
+    if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBLsuGather) {
+      // Warps 6-9 copy the chunk's token rows from hidden with 16-byte
+      // cp.async into the 128-byte-swizzled layout the MMA reads (16-byte
+      // chunk c of row r at r*128 + ((c ^ (r % 8)) * 16)). Thread (w, l) moves
+      // chunk l % 8 of rows p*16 + w*4 + l/8, p = 0..7. Each thread's copies
+      // arrive on the stage's barrier by themselves when they land
+      // (cp.async.mbarrier.arrive.noinc, 128 arrivals per stage); the MMA
+      // thread then fences the generic-to-async proxy before reading.
+      const int w = warp - 6, c16 = lane & 7;
+      const uint16_t* src[8];
+      const uint16_t* nxt[8];
+      auto fetch_rows = [&](int tl, const uint16_t* (&rows)[8]) {
+        int e, m, row0, nrows;
+        if (tl < total_tiles) decode_tile<BN>(tl, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int r = p * 16 + w * 4 + (lane >> 3);
+          const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
+          rows[p] = f < a.Tk ? a.hidden + (size_t)(f / a.top_k) * a.K + c16 * 8 : nullptr;
+        }
+      };
+      fetch_rows(blockIdx.x, nxt);
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        if (aborted(&abort_s)) break;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) src[p] = nxt[p];
+        fetch_rows(tile + gridDim.x, nxt);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (lane == 0) ok = mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            if (lane == 0) signal_abort(&abort_s, a.err);
+            break;
+          }
+          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int r = p * 16 + w * 4 + (lane >> 3);
+            const uint32_t dst = st + r * 128 + ((c16 ^ (r & 7)) << 4);
+            cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * kGK : a.hidden,
+                             src[p] != nullptr);
+          }
+          cp_async_arrive_noinc(smem_u32(&fullB[s]));
+          if (++s == SB) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      cp_async_wait<0>();  // no copy of this thread is in flight when the CTA ends
+    } else if (warp != 6) {
+      // Warps 7-9 help only on the cp.async path.
+    } else if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBTmaGather) {
       // Token rows are gathered straight from hidden: lane i loads rows
       // 4i..4i+3 of the chunk with one tile::gather4 per stage. The rows of the
       // next tile are fetched one tile ahead so their latency is hidden.
@@ -211,30 +332,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fetch_rows(tile + gridDim.x, nxt);
         int e, m, row0, nrows;
         decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
-        const int wrow0 = e * a.w_rows + m * a.m_step;
-        const int wrow1 = wrow0 + a.a1_off;
         const int n_g4 = ((nrows + 15) & ~15) / 4;  // rows the MMA reads, 4 per gather
-        const uint32_t bytes = 2 * Cfg::kABytes + n_g4 * 4 * kGK * 2;
+        const uint32_t bytes = n_g4 * 4 * kGK * 2;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
+          if (lane == 0) ok = mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             if (lane == 0) signal_abort(&abort_s, a.err);
             break;
           }
-          const uint32_t st = smem_base + s * Cfg::kStageBytes;
-          const uint32_t fb = smem_u32(&full[s]);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
-            tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
-          }
+          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
+          const uint32_t fb = smem_u32(&fullB[s]);
+          if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
           __syncwarp();
           if (lane < n_g4)
-            tma_gather4(st + 2 * Cfg::kABytes + lane * 4 * kGK * 2, &tmX, fb, kb * kGK, rows[0],
-                        rows[1], rows[2], rows[3], pol_x);
-          if (++s == STAGES) {
+            tma_gather4(st + lane * 4 * kGK * 2, &tmX, fb, kb * kGK, rows[0], rows[1], rows[2],
+                        rows[3], pol_x);
+          if (++s == SB) {
             s = 0;
             ph ^= 1u;
           }
@@ -246,22 +361,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (aborted(&abort_s)) break;
         int e, m, row0, nrows;
         decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
-        const int wrow0 = e * a.w_rows + m * a.m_step;
-        const int wrow1 = wrow0 + a.a1_off;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
+          if (!mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u)) {
             signal_abort(&abort_s, a.err);
             ok = false;
             break;
           }
-          const uint32_t st = smem_base + s * Cfg::kStageBytes;
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
-          tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
-          tma_load_2d(st + 2 * Cfg::kABytes, &tmX, fb, kb * kGK, row0, pol_x);
-          if (++s == STAGES) {
+          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
+          const uint32_t fb = smem_u32(&fullB[s]);
+          mbar_arrive_expect_tx(fb, Cfg::kBStageBytes);
+          tma_load_2d(st, &tmX, fb, kb * kGK, row0, pol_x);
+          if (++s == SB) {
             s = 0;
             ph ^= 1u;
           }
@@ -272,9 +383,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer ---
     if (lane == 0) {
-      const int nk = a.K / kGK;
-      int s = 0;
-      uint32_t ph = 0;
+      int sa = 0, sb = 0;
+      uint32_t pha = 0, phb = 0;
       int it = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
         if (aborted(&abort_s)) break;
@@ -293,26 +403,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d1 = d0 + BN;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(smem_u32(&full[s]), ph)) {
+          if (!mbar_wait(smem_u32(&fullA[sa]), pha) || !mbar_wait(smem_u32(&fullB[sb]), phb)) {
             signal_abort(&abort_s, a.err);
             ok = false;
             break;
           }
+          // Rows written by cp.async (generic proxy) are read by the MMA (async proxy).
+          if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBLsuGather) fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t st = smem_base + s * Cfg::kStageBytes;
+          const uint32_t sta = smem_base + sa * Cfg::kAStageBytes;
+          const uint32_t stb = smem_base + Cfg::kBOffset + sb * Cfg::kBStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kGK / 16; ++kk) {
-            const uint64_t da0 = sdesc_k128(st + kk * 32);
-            const uint64_t da1 = sdesc_k128(st + Cfg::kABytes + kk * 32);
-            const uint64_t db = sdesc_k128(st + 2 * Cfg::kABytes + kk * 32);
+            const uint64_t da0 = sdesc_k128(sta + kk * 32);
+            const uint64_t da1 = sdesc_k128(sta + Cfg::kABytes + kk * 32);
+            const uint64_t db = sdesc_k128(stb + kk * 32);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             umma_bf16(d0, da0, db, idesc, acc);
             umma_bf16(d1, da1, db, idesc, acc);
           }
-          umma_commit(smem_u32(&empty[s]));  // frees the stage once these MMAs are done
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
+          umma_commit(smem_u32(&emptyA[sa]));  // frees both stages once these MMAs are done
+          umma_commit(smem_u32(&emptyB[sb]));
+          if (++sa == SA) {
+            sa = 0;
+            pha ^= 1u;
+          }
+          if (++sb == SB) {
+            sb = 0;
+            phb ^= 1u;
           }
         }
         if (!ok) break;
@@ -323,7 +441,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(smem_u32(done), 0)) signal_abort(&abort_s, a.err);
     }
   } else {
-    // ---------------------------------------------------------- epilogue ---
+    // ----------------------------------------------------- epilogue (2-5) ---
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
     const int r_in = q * 32 + lane;
     int it = 0;
@@ -462,16 +580,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int SA, int SB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
                        int top_k, int E, int N, int K, long long capacity, int num_sms,
                        unsigned* err, cudaStream_t st) {
-  using Cfg = GemmCfg<BN, STAGES>;
+  using Cfg = GemmCfg<MODE, BN, SA, SB>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, SA, SB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -491,7 +609,11 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   // With more than about half a chunk of rows per expert on average, several
   // token chunks read each weight tile: keep the weights at normal priority.
   a.w_evict_first = (long long)T * top_k <= (long long)E * (BN / 2) ? 1 : 0;
-  a.gather_rows = (MODE == MM_GEMM_GATE_UP && x_is_hidden) ? 1 : 0;
+  a.hidden = x_is_hidden ? X : nullptr;
+  if (MODE == MM_GEMM_GATE_UP && x_is_hidden)
+    a.b_mode = gate_up_gathers_rows(T, top_k, E) ? kBTmaGather : kBLsuGather;
+  else
+    a.b_mode = kBTma;
   if (MODE == MM_GEMM_GATE_UP) {
     a.w_rows = 2 * N;
     a.m_step = kGM;
@@ -507,37 +629,15 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM)) return cudaErrorInvalidValue;
   // Gathered rows: X = hidden [T, K], one row per box; otherwise X holds the
   // token rows in segment order [capacity, K].
-  const bool ok_x = a.gather_rows ? make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1)
-                                  : make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN);
+  // gather4 reads hidden [T, K] one row per box row; 2-D boxes read rows in
+  // segment order [capacity, K]; the cp.async path does not use the map.
+  const bool ok_x = a.b_mode == kBTma ? make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN)
+                                      : make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1);
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  grouped_gemm_kernel<MODE, BN, STAGES><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
+  grouped_gemm_kernel<MODE, BN, SA, SB><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
   return cudaGetLastError();
-}
-
-// x_sorted[r] = hidden[sorted[r] / k] (zeros for padding rows), one warp per
-// row, 16-byte loads and stores.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ hidden,
-                                                          const int32_t* __restrict__ sorted,
-                                                          const int32_t* __restrict__ offsets,
-                                                          int E, int Tk, int k, int H,
-                                                          uint16_t* __restrict__ xs) {
-  const int m_pad = offsets[E];
-  const int lane = threadIdx.x & 31;
-  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
-  const int vec = H / 8;
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < m_pad;
-       r += nw) {
-    const int f = sorted[r];
-    uint4* dst = reinterpret_cast<uint4*>(xs + r * H);
-    if (f < Tk) {
-      const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(f / k) * H);
-      for (int c = lane; c < vec; c += 32) dst[c] = __ldg(src + c);
-    } else {
-      for (int c = lane; c < vec; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
 }
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
@@ -562,24 +662,16 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
+  // Few rows per expert (gather4, weight-streaming bound): deep weight ring.
+  // Many rows per expert (cp.async rows): a deeper token ring.
+  if (mode == MM_GEMM_GATE_UP && x_is_hidden && gate_up_gathers_rows(T, top_k, E))
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 5, 3>(X, x_is_hidden, W, C, sorted, offsets, topk_w,
+                                                  T, top_k, E, N, K, capacity, num_sms, err, st);
   if (mode == MM_GEMM_GATE_UP)
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 4>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 5>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
                                                top_k, E, N, K, capacity, num_sms, err, st);
-  return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
+  return launch_cfg<MM_GEMM_DOWN, 128, 4, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
                                           K, capacity, num_sms, err, st);
-}
-
-cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
-                               const int32_t* offsets, int E, int T, int top_k, int H,
-                               long long capacity, uint16_t* x_sorted, int num_sms,
-                               cudaStream_t st) {
-  long long blocks = (capacity + 7) / 8;
-  const long long cap_blocks = (long long)num_sms * 8;
-  if (blocks > cap_blocks) blocks = cap_blocks;
-  if (blocks < 1) blocks = 1;
-  gather_rows_kernel<<<(int)blocks, 256, 0, st>>>(hidden, sorted, offsets, E, T * top_k, top_k, H,
-                                                  x_sorted);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

@@ -60,24 +60,27 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, cudaStream_t st);
 
-// Whether the gate_up GEMM should gather token rows from hidden itself
-// (few rows per expert) instead of reading a copy in segment order.
+// Whether the gate_up GEMM gathers token rows with TMA tile::gather4 (few rows
+// per expert) rather than with cp.async loader warps.
 bool gate_up_gathers_rows(int T, int top_k, int E);
-
-// x_sorted[r] = hidden[sorted[r] / top_k] for r < offsets[E] (zeros for padding).
-cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
-                               const int32_t* offsets, int E, int T, int top_k, int H,
-                               long long capacity, uint16_t* x_sorted, int num_sms,
-                               cudaStream_t st);
 
 // Grouped GEMM on tcgen05. mode 0: C = act bf16 [capacity, N] = silu(gate) *
 // up; X = hidden [T, K] with rows gathered through sorted / top_k when
-// x_is_hidden, else X = token rows already in segment order [capacity, K].
+// x_is_hidden (always, from the library's entry points), else X = token rows
+// already in segment order [capacity, K].
 // mode 1: X = act [capacity, K], C = fp32 acc [T, N] += topk_w * (X W^T).
 cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st);
+
+// The same grouped GEMMs on CTA pairs (tcgen05 cta_group::2), for batches with
+// many rows per expert; X = token rows in segment order [capacity, K].
+cudaError_t launch_grouped_gemm_pair(int mode, const uint16_t* X, const uint16_t* W, void* C,
+                                     const int32_t* sorted, const int32_t* offsets,
+                                     const float* topk_w, int T, int top_k, int E, int N, int K,
+                                     long long capacity, int num_sms, unsigned* err,
+                                     cudaStream_t st);
 
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
