@@ -23,10 +23,9 @@
 // and no permuted copy of the activations is ever written.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over a static tile
-// stride): warp 0 = weight (A) TMA producer with a deep ring, warps 6-9 =
-// token (B) producer (warp 6 alone for TMA), warp 1 = TMEM allocator + MMA
-// issuer, warps 2-5 = epilogue (each reads its 32-lane quarter of tensor
-// memory).
+// stride): warp 0 = weight (A) TMA producer, warps 6-9 = token (B) producer
+// (warp 6 alone for TMA), warp 1 = TMEM allocator + MMA issuer, warps 2-5 =
+// epilogue (each reads its 32-lane quarter of tensor memory).
 // Two accumulator buffers let the epilogue of one tile overlap the
 // main loop of the next.
 //
@@ -69,18 +68,19 @@ constexpr int kBTma = 0;        // 2-D TMA boxes of rows already in segment orde
 constexpr int kBTmaGather = 1;  // TMA tile::gather4 from hidden (few rows per expert)
 constexpr int kBLsuGather = 2;  // four warps of cp.async from hidden (many rows per expert)
 
-// Two shared-memory rings: SA stages of weight tiles (A0 + A1, 32 KB) and SB
-// stages of token tiles (BN rows). The weights are the DRAM stream, so their
-// ring is the deep one; the token rows mostly hit L2.
-template <int MODE, int BN, int SA, int SB>
+// One shared-memory ring of S stages; a stage holds the two weight tiles (A0,
+// A1: 32 KB) and the token tile (BN rows) of one K step. The weight producer
+// and the token producer fill a stage independently (each arrives on its
+// full barrier), but both wait for the same stage to be freed, so loads are
+// issued in the order the MMA needs them.
+template <int MODE, int BN, int S>
 struct GemmCfg {
   static constexpr int kABytes = kGM * kGK * 2;        // one 128-row weight tile
-  static constexpr int kAStageBytes = 2 * kABytes;     // A0 + A1
-  static constexpr int kBStageBytes = BN * kGK * 2;
+  static constexpr int kBBytes = BN * kGK * 2;
+  static constexpr int kStageBytes = 2 * kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 4 * BN;  // 2 buffers x (D0, D1) x BN columns
   static constexpr int kEpiBytes = MODE == MM_GEMM_DOWN ? 4 * 32 * 33 * 4 : 0;  // transpose tiles
-  static constexpr int kBOffset = SA * kAStageBytes;
-  static constexpr int kEpiOffset = kBOffset + SB * kBStageBytes;
+  static constexpr int kEpiOffset = S * kStageBytes;
   static constexpr int kSmemBytes = kEpiOffset + kEpiBytes + 1024;
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
@@ -133,13 +133,13 @@ __device__ __forceinline__ void signal_abort(int* flag, unsigned* err) {
   atomicOr(err, kDevErrTimeout);
 }
 
-template <int MODE, int BN, int SA, int SB>
+template <int MODE, int BN, int S>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs a) {
-  using Cfg = GemmCfg<MODE, BN, SA, SB>;
+  using Cfg = GemmCfg<MODE, BN, S>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[2 * SA + 2 * SB + 5];
+  __shared__ __align__(8) uint64_t bars[2 * S + 5];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   __shared__ int off_s[kMaxExperts + 1];
@@ -182,22 +182,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t smem_base = (raw_addr + 1023u) & ~1023u;
   float* epi_tile =
       reinterpret_cast<float*>(smem_raw + (smem_base - raw_addr) + Cfg::kEpiOffset);
-  uint64_t* fullA = bars;
-  uint64_t* emptyA = fullA + SA;
-  uint64_t* fullB = emptyA + SA;
-  uint64_t* emptyB = fullB + SB;
-  uint64_t* tfull = emptyB + SB;
+  uint64_t* full = bars;
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;
   uint64_t* tempty = tfull + 2;
   uint64_t* done = tempty + 2;
 
   if (tid == 0) {
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(smem_u32(&fullA[s]), 1);
-      mbar_init(smem_u32(&emptyA[s]), 1);
-    }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(smem_u32(&fullB[s]), a.b_mode == kBLsuGather ? 128 : 1);  // one per loader thread
-      mbar_init(smem_u32(&emptyB[s]), 1);
+    for (int s = 0; s < S; ++s) {
+      // the weight producer + the token side (one TMA producer or 128 loaders)
+      mbar_init(smem_u32(&full[s]), 1 + (a.b_mode == kBLsuGather ? 128 : 1));
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -234,17 +229,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int wrow1 = wrow0 + a.a1_off;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(smem_u32(&emptyA[s]), ph ^ 1u)) {
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
             signal_abort(&abort_s, a.err);
             ok = false;
             break;
           }
-          const uint32_t st = smem_base + s * Cfg::kAStageBytes;
-          const uint32_t fb = smem_u32(&fullA[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kAStageBytes);
+          const uint32_t st = smem_base + s * Cfg::kStageBytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, 2 * Cfg::kABytes);
           tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
           tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
-          if (++s == SA) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
@@ -286,13 +281,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int p = 0; p < 8; ++p) src[p] = nxt[p];
         fetch_rows(tile + gridDim.x, nxt);
         for (int kb = 0; kb < nk; ++kb) {
-          if (lane == 0) ok = mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u);
+          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             if (lane == 0) signal_abort(&abort_s, a.err);
             break;
           }
-          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
+          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
 #pragma unroll
           for (int p = 0; p < 8; ++p) {
             const int r = p * 16 + w * 4 + (lane >> 3);
@@ -300,8 +295,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * kGK : a.hidden,
                              src[p] != nullptr);
           }
-          cp_async_arrive_noinc(smem_u32(&fullB[s]));
-          if (++s == SB) {
+          cp_async_arrive_noinc(smem_u32(&full[s]));
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
@@ -336,20 +331,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t bytes = n_g4 * 4 * kGK * 2;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (lane == 0) ok = mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u);
+          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
             if (lane == 0) signal_abort(&abort_s, a.err);
             break;
           }
-          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
-          const uint32_t fb = smem_u32(&fullB[s]);
+          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
+          const uint32_t fb = smem_u32(&full[s]);
           if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
           __syncwarp();
           if (lane < n_g4)
             tma_gather4(st + lane * 4 * kGK * 2, &tmX, fb, kb * kGK, rows[0], rows[1], rows[2],
                         rows[3], pol_x);
-          if (++s == SB) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
@@ -363,16 +358,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(smem_u32(&emptyB[s]), ph ^ 1u)) {
+          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
             signal_abort(&abort_s, a.err);
             ok = false;
             break;
           }
-          const uint32_t st = smem_base + Cfg::kBOffset + s * Cfg::kBStageBytes;
-          const uint32_t fb = smem_u32(&fullB[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kBStageBytes);
+          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, Cfg::kBBytes);
           tma_load_2d(st, &tmX, fb, kb * kGK, row0, pol_x);
-          if (++s == SB) {
+          if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
@@ -383,8 +378,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer ---
     if (lane == 0) {
-      int sa = 0, sb = 0;
-      uint32_t pha = 0, phb = 0;
+      int s = 0;
+      uint32_t ph = 0;
       int it = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
         if (aborted(&abort_s)) break;
@@ -403,7 +398,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d1 = d0 + BN;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(smem_u32(&fullA[sa]), pha) || !mbar_wait(smem_u32(&fullB[sb]), phb)) {
+          if (!mbar_wait(smem_u32(&full[s]), ph)) {
             signal_abort(&abort_s, a.err);
             ok = false;
             break;
@@ -411,26 +406,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // Rows written by cp.async (generic proxy) are read by the MMA (async proxy).
           if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBLsuGather) fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t sta = smem_base + sa * Cfg::kAStageBytes;
-          const uint32_t stb = smem_base + Cfg::kBOffset + sb * Cfg::kBStageBytes;
+          const uint32_t st = smem_base + s * Cfg::kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kGK / 16; ++kk) {
-            const uint64_t da0 = sdesc_k128(sta + kk * 32);
-            const uint64_t da1 = sdesc_k128(sta + Cfg::kABytes + kk * 32);
-            const uint64_t db = sdesc_k128(stb + kk * 32);
+            const uint64_t da0 = sdesc_k128(st + kk * 32);
+            const uint64_t da1 = sdesc_k128(st + Cfg::kABytes + kk * 32);
+            const uint64_t db = sdesc_k128(st + 2 * Cfg::kABytes + kk * 32);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             umma_bf16(d0, da0, db, idesc, acc);
             umma_bf16(d1, da1, db, idesc, acc);
           }
-          umma_commit(smem_u32(&emptyA[sa]));  // frees both stages once these MMAs are done
-          umma_commit(smem_u32(&emptyB[sb]));
-          if (++sa == SA) {
-            sa = 0;
-            pha ^= 1u;
-          }
-          if (++sb == SB) {
-            sb = 0;
-            phb ^= 1u;
+          umma_commit(smem_u32(&empty[s]));  // frees the stage once these MMAs are done
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
           }
         }
         if (!ok) break;
@@ -580,16 +569,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BN, int SA, int SB>
+template <int MODE, int BN, int S>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
                        int top_k, int E, int N, int K, long long capacity, int num_sms,
                        unsigned* err, cudaStream_t st) {
-  using Cfg = GemmCfg<MODE, BN, SA, SB>;
+  using Cfg = GemmCfg<MODE, BN, S>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, SA, SB>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -636,7 +625,7 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  grouped_gemm_kernel<MODE, BN, SA, SB><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
+  grouped_gemm_kernel<MODE, BN, S><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
   return cudaGetLastError();
 }
 
@@ -662,15 +651,10 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
-  // Few rows per expert (gather4, weight-streaming bound): deep weight ring.
-  // Many rows per expert (cp.async rows): a deeper token ring.
-  if (mode == MM_GEMM_GATE_UP && x_is_hidden && gate_up_gathers_rows(T, top_k, E))
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 5, 3>(X, x_is_hidden, W, C, sorted, offsets, topk_w,
-                                                  T, top_k, E, N, K, capacity, num_sms, err, st);
   if (mode == MM_GEMM_GATE_UP)
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 5>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 4>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
                                                top_k, E, N, K, capacity, num_sms, err, st);
-  return launch_cfg<MM_GEMM_DOWN, 128, 4, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
+  return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
                                           K, capacity, num_sms, err, st);
 }
 

@@ -74,14 +74,6 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st);
 
-// The same grouped GEMMs on CTA pairs (tcgen05 cta_group::2), for batches with
-// many rows per expert; X = token rows in segment order [capacity, K].
-cudaError_t launch_grouped_gemm_pair(int mode, const uint16_t* X, const uint16_t* W, void* C,
-                                     const int32_t* sorted, const int32_t* offsets,
-                                     const float* topk_w, int T, int top_k, int E, int N, int K,
-                                     long long capacity, int num_sms, unsigned* err,
-                                     cudaStream_t st);
-
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
                             cudaStream_t st);

@@ -8,10 +8,12 @@
 // latency-bound. Here a thread-block cluster of KS CTAs (KS <= 8) shares a
 // tile: CTA r loads and multiplies only the K-slice [r*H/KS, (r+1)*H/KS) with
 // all its chunks in flight at once (warp-level mma.sync, fp32 accumulate),
-// keeps its partial logits in shared memory, and after a cluster barrier
-// each CTA sums the KS partials of 64/KS tokens through distributed shared
-// memory in rank order (so the result does not depend on timing) and runs
-// the softmax and k rounds of warp arg-max. Logits never reach global memory.
+// then pushes the partial logits of each token to the CTA that finishes that
+// token (remote shared-memory stores into its now free staging buffers).
+// After a cluster barrier each CTA sums the KS partials of its 64/KS tokens
+// in rank order from its own shared memory (so the result does not depend on
+// timing) and runs the softmax and k rounds of warp arg-max (one token per
+// warp). Logits never reach global memory.
 //
 // When one cluster covers the whole batch (T <= 64), CTA 0 of the cluster
 // also groups the tokens by expert after the final cluster barrier (which
@@ -28,7 +30,8 @@ namespace {
 constexpr int kRtTok = 64;        // tokens per cluster tile
 constexpr int kRtKc = 64;         // K per cp.async chunk
 constexpr int kRtLd = kRtKc + 8;  // padded smem row (bf16): 144 B, conflict-free ldmatrix
-constexpr int kRtThreads = 128;
+constexpr int kRtThreads = 256;  // 8 warps: 4 run the MMAs, all 8 finish tokens
+constexpr int kRtMmaWarps = 4;   // 16 token rows each
 constexpr int kRtBufs = 4;        // chunks in flight per CTA
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -42,14 +45,16 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
-// Loads a float from the shared memory of CTA `rank` of this cluster, at the
-// offset `local` has in this CTA.
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+// Address in CTA `rank` of this cluster of the shared variable at `local`.
+__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
   uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ void st_dsmem_v2(uint32_t cluster_addr, float a, float b) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(cluster_addr), "f"(a), "f"(b)
+               : "memory");
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -92,7 +97,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // [kRtBufs][kRtTok][kRtLd]
   uint16_t* ws = xs + kRtBufs * kRtTok * kRtLd;       // [kRtBufs][EP][kRtLd]
-  float* part = reinterpret_cast<float*>(smem);       // after the GEMM: [kRtTok][EP + 1]
+  float* recv = reinterpret_cast<float*>(smem);       // after the GEMM: [KS][64/KS][EP]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
@@ -138,19 +143,21 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
     __syncthreads();
     const uint16_t* xb = xs + (c % kRtBufs) * kRtTok * kRtLd;
     const uint16_t* wb = ws + (c % kRtBufs) * EP * kRtLd;
+    if (warp < kRtMmaWarps) {
 #pragma unroll
-    for (int kk = 0; kk < kRtKc / 16; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(smem_u32(xb + (warp * 16 + (lane & 15)) * kRtLd + kk * 16 + (lane >> 4) * 8), a0,
-                  a1, a2, a3);
+      for (int kk = 0; kk < kRtKc / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(smem_u32(xb + (warp * 16 + (lane & 15)) * kRtLd + kk * 16 + (lane >> 4) * 8),
+                    a0, a1, a2, a3);
 #pragma unroll
-      for (int j2 = 0; j2 < EP / 16; ++j2) {
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(smem_u32(wb + (j2 * 16 + (lane & 7) + ((lane >> 4) << 3)) * kRtLd + kk * 16 +
-                             ((lane >> 3) & 1) * 8),
-                    b0, b1, b2, b3);
-        mma_bf16_16816(acc[2 * j2], a0, a1, a2, a3, b0, b1);
-        mma_bf16_16816(acc[2 * j2 + 1], a0, a1, a2, a3, b2, b3);
+        for (int j2 = 0; j2 < EP / 16; ++j2) {
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(smem_u32(wb + (j2 * 16 + (lane & 7) + ((lane >> 4) << 3)) * kRtLd +
+                               kk * 16 + ((lane >> 3) & 1) * 8),
+                      b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * j2], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[2 * j2 + 1], a0, a1, a2, a3, b2, b3);
+        }
       }
     }
     __syncthreads();
@@ -159,24 +166,43 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
   cp_async_wait<0>();
   __syncthreads();
 
-  // Partial logits of this K-slice -> shared [token][expert].
-  {
+  // Every CTA of the cluster has finished with its staging buffers; they now
+  // receive partial logits: recv[src][rr][e] holds CTA src's partial sum for
+  // token rr of this CTA's share (64/KS tokens). Each CTA pushes its rows to
+  // their owners with remote stores, so the reduction below reads only local
+  // shared memory.
+  const int per = kRtTok / ks;  // tokens each CTA finishes
+  if (ks > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  if (warp < kRtMmaWarps) {
     const int r0 = warp * 16 + (lane >> 2), c0 = 2 * (lane & 3);
 #pragma unroll
-    for (int j = 0; j < EP / 8; ++j) {
-      part[r0 * (EP + 1) + j * 8 + c0] = acc[j][0];
-      part[r0 * (EP + 1) + j * 8 + c0 + 1] = acc[j][1];
-      part[(r0 + 8) * (EP + 1) + j * 8 + c0] = acc[j][2];
-      part[(r0 + 8) * (EP + 1) + j * 8 + c0 + 1] = acc[j][3];
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + 8 * h;
+      const int owner = r / per;
+      float* row = recv + ((int)rank * per + (r - owner * per)) * EP;
+      if (ks > 1) {
+        const uint32_t rbase = map_rank(smem_u32(row), (uint32_t)owner);
+#pragma unroll
+        for (int j = 0; j < EP / 8; ++j)
+          st_dsmem_v2(rbase + (j * 8 + c0) * 4, acc[j][2 * h], acc[j][2 * h + 1]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < EP / 8; ++j) {
+          row[j * 8 + c0] = acc[j][2 * h];
+          row[j * 8 + c0 + 1] = acc[j][2 * h + 1];
+        }
+      }
     }
   }
   if (ks > 1)
-    cluster_sync();  // every CTA's partials are visible cluster-wide
+    cluster_sync();  // all pushes have landed
   else
     __syncthreads();
 
   constexpr int Q = EP / 32;  // logits per lane
-  const int per = kRtTok / ks;  // tokens this CTA finishes
   for (int rr = warp; rr < per; rr += kRtThreads / 32) {
     const int r = (int)rank * per + rr, t = t0 + r;
     if (t >= T) break;
@@ -188,8 +214,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       if (e < E) {
         float v = 0.f;
         for (int src = 0; src < ks; ++src)  // fixed order: deterministic sum
-          v += ks > 1 ? ld_dsmem_f32(part + r * (EP + 1) + e, (uint32_t)src)
-                      : part[r * (EP + 1) + e];
+          v += recv[(src * per + rr) * EP + e];
         l[q] = v + (bias != nullptr ? bias[e] : 0.f);
       }
     }
@@ -208,29 +233,30 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
 
     // k rounds of warp arg-max: the larger logit wins, equal logits go to the
-    // lower expert id.
+    // lower expert id. A logit is compared as an order-preserving uint32 key
+    // (exact: -0 is first folded into +0), so one warp-wide max reduction
+    // finds the best value and one min reduction picks the lowest id
+    // holding it.
+    uint32_t key[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      const uint32_t b = __float_as_uint(l[q] + 0.0f);
+      key[q] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
     uint32_t sel = 0;
     for (int round = 0; round < top_k; ++round) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
+      uint32_t bk = 0;
+      int bq = Q;  // none
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {  // ascending ids: strict '>' keeps the lower id on ties
-        const int e = lane + 32 * q;
-        if (e < E && !((sel >> q) & 1u) && (bi == 0x7fffffff || l[q] > bv)) {
-          bv = l[q];
-          bi = e;
+      for (int q = 0; q < Q; ++q)  // ascending ids: strict '>' keeps the lower id on ties
+        if (lane + 32 * q < E && !((sel >> q) & 1u) && (bq == Q || key[q] > bk)) {
+          bk = key[q];
+          bq = q;
         }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) sel |= 1u << (bi >> 5);
+      const uint32_t m = __reduce_max_sync(0xffffffffu, bq < Q ? bk : 0u);
+      const uint32_t cand = (bq < Q && bk == m) ? static_cast<uint32_t>(bq * 32 + lane) : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if ((int)(win & 31u) == lane) sel |= 1u << (win >> 5);
     }
 
     // Probabilities of the selected experts, renormalised if asked.
@@ -260,15 +286,16 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
       base += __popc(bal);
     }
   }
-  // Keeps this CTA's partials alive until every reader is done, and publishes
-  // every CTA's ids to the cluster.
-  if (ks > 1)
-    cluster_sync();
-  else
-    __syncthreads();
-  if (fa.sorted != nullptr && rank == 0)
-    alignblk::align_one_block(ids_out, T, top_k, E, fa.block_m, fa.capacity, fa.sorted,
-                              fa.offsets, fa.counts, fa.err, smem);
+  // The grouping (T <= 64) needs every CTA's ids: one more cluster barrier.
+  if (fa.sorted != nullptr) {
+    if (ks > 1)
+      cluster_sync();
+    else
+      __syncthreads();
+    if (rank == 0)
+      alignblk::align_one_block(ids_out, T, top_k, E, fa.block_m, fa.capacity, fa.sorted,
+                                fa.offsets, fa.counts, fa.err, smem);
+  }
 }
 
 template <int EP>
@@ -276,8 +303,8 @@ cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const fl
                       int H, int E, int top_k, int renorm, int32_t* ids, float* w, float* zero_buf,
                       long long zero_count, const AlignOut& fa, cudaStream_t st) {
   const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
-  const size_t part_bytes = (size_t)kRtTok * (EP + 1) * sizeof(float);
-  const size_t smem = gemm_bytes > part_bytes ? gemm_bytes : part_bytes;
+  const size_t recv_bytes = (size_t)kRtTok * EP * sizeof(float);
+  const size_t smem = gemm_bytes > recv_bytes ? gemm_bytes : recv_bytes;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
