@@ -194,6 +194,24 @@ int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w,
                       uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The dense SwiGLU MLP, through the same grouped-GEMM kernels: out =
+ * down_proj(silu(gate_proj(x)) * up_proj(x)) for every token ("模型与权重加载",
+ * GatedMLP; Qwen3 dense layers, and the MoE model's mlp_only_layers named in
+ * its ModelConfig). Equal to mm_moe_forward with one expert, top_k = 1 and a
+ * routing weight of 1, without the router.
+ *
+ * hidden [T,H] bf16, w_gate_up [2I,H] bf16 (gate rows first), w_down [H,I]
+ * bf16; out [T,H] bf16 (one rounding of the fp32 result). Uses the internal
+ * workspace (mm_gated_mlp_workspace_size bytes), so calls on one device must
+ * not overlap. T == 0 is a no-op.
+ */
+int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16_t* w_down,
+                 int T, int H, int I, uint16_t* out, void* stream);
+
+/* Bytes of internal workspace mm_gated_mlp uses for these sizes (-1 if invalid). */
+int64_t mm_gated_mlp_workspace_size(int T, int H, int I);
+
+/*
  * Stage timing of mm_moe_forward_ex, for profiling. Same arguments, plus
  * `events`: a host array of MM_PROFILE_EVENTS cudaEvent_t handles (created
  * by the caller with timing enabled). events[i] is recorded on `stream`

@@ -40,6 +40,8 @@ SIGNATURES = {
     "mm_moe_forward_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mm_moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
                                      _P]),
+    "mm_gated_mlp": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "mm_gated_mlp_workspace_size": (_I64, [_I, _I, _I]),
     "mm_poll_device_status": (_I, [_P]),
     "mm_shutdown": (None, []),
 }
@@ -207,6 +209,23 @@ def mm_moe_forward(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool
                                    T, H, E, I, top_k, int(bool(renorm)),
                                    _ptr(out, torch.bfloat16, "out"), ws_ptr, ws_bytes,
                                    _stream(stream)), "mm_moe_forward_ex")
+    return out
+
+
+def mm_gated_mlp_workspace_size(T: int, H: int, I: int) -> int:
+    return int(lib().mm_gated_mlp_workspace_size(T, H, I))
+
+
+def mm_gated_mlp(hidden, w_gate_up, w_down, out=None, stream=None):
+    """Dense SwiGLU MLP through the grouped-GEMM kernels; returns out [T, H] bf16."""
+    T, H = hidden.shape
+    I = w_down.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    _check(lib().mm_gated_mlp(_ptr(hidden, torch.bfloat16, "hidden"),
+                              _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+                              _ptr(w_down, torch.bfloat16, "w_down"), T, H, I,
+                              _ptr(out, torch.bfloat16, "out"), _stream(stream)), "mm_gated_mlp")
     return out
 
 

@@ -12,9 +12,9 @@
 // Each block first copies its tokens' ids to shared memory (one coalesced
 // pass), then works from there.
 // Small batches (T <= 1024 and T*k <= 8192): one block does histogram, scan
-// and scatter in a single launch. Otherwise: three launches over blocks of
-// 256 tokens (per-block counts, one-block scan, scatter); no block ever waits
-// on another.
+// and scatter in a single launch. Otherwise: two launches over blocks of 256
+// tokens (per-block counts; then each block derives its own slot bases from
+// all blocks' counts and scatters); no block ever waits on another.
 #include "align_block.cuh"
 
 namespace mm {
@@ -49,56 +49,85 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_count_kernel(
   }
 }
 
-// One block: per expert, exclusive scan of the block counts (in place, so
-// block_counts becomes each block's base slot), padded offsets, padding.
-__global__ void __launch_bounds__(256) align_scan_kernel(int nblocks, int T, int k, int E, int bm,
-                                                         long long capacity,
-                                                         int32_t* __restrict__ block_counts,
-                                                         int32_t* __restrict__ sorted,
-                                                         int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ counts) {
-  __shared__ int tot_s[kMaxExperts];
-  __shared__ int off_s[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblocks; ++b) {
-      const int c = block_counts[b * E + e];
-      block_counts[b * E + e] = run;
-      run += c;
-    }
-    tot_s[e] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) warp_scan_padded(tot_s, E, bm, off_s);
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-    offsets[e] = off_s[e];
-    if (e < E && counts != nullptr) counts[e] = tot_s[e];
-  }
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    for (int b = 0; b < nblocks; ++b) block_counts[b * E + e] += off_s[e];
-  fill_padding(off_s, tot_s, E, capacity, T * k, sorted);
-}
-
-__global__ void __launch_bounds__(kAlignBlockTokens) align_scatter_kernel(
-    const int32_t* __restrict__ ids, int T, int k, int E, const int32_t* __restrict__ block_base,
-    int32_t* __restrict__ sorted, unsigned* err) {
+// Per block: each expert's slot base for this block's tokens (the expert's
+// padded offset plus the counts of all earlier blocks, summed here with
+// independent loads), then the stable scatter. Block 0 also writes the
+// offsets, the counts and the padding sentinels.
+__global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int bm, long long capacity, int nblocks,
+    const int32_t* __restrict__ block_counts, int32_t* __restrict__ sorted,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ counts) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int W = kAlignBlockTokens / 32;
   const AlignSmem S = carve(smem, W, E);
+  int* base_s = reinterpret_cast<int*>(smem + align_smem_bytes(W, E, k));  // [E]
   const int tok0 = blockIdx.x * kAlignBlockTokens;
   stage_ids(ids, T, k, tok0, S.ids);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) S.off[e] = block_base[blockIdx.x * E + e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+#pragma unroll 8
+    for (int b = 0; b < nblocks; ++b) {
+      const int c = __ldg(block_counts + (size_t)b * E + e);
+      before += b < (int)blockIdx.x ? c : 0;
+      total += c;
+    }
+    S.tot[e] = total;
+    base_s[e] = before;
+  }
   __syncthreads();
+  if (threadIdx.x < 32) warp_scan_padded(S.tot, E, bm, S.off);
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+      offsets[e] = S.off[e];
+      if (e < E && counts != nullptr) counts[e] = S.tot[e];
+    }
+    fill_padding(S.off, S.tot, E, capacity, T * k, sorted);
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) base_s[e] += S.off[e];
   // Bad ids were already flagged by the count kernel.
   block_ballots(S.ids, T, k, E, tok0, S.bal, nullptr);
   __syncthreads();
   warp_prefix(S.bal, W, E, S.pre, S.tot);
   __syncthreads();
-  block_scatter(S.ids, T, k, E, tok0, S.bal, S.pre, S.off, sorted);
+  block_scatter(S.ids, T, k, E, tok0, S.bal, S.pre, base_s, sorted);
+}
+
+// The grouping of a dense MLP: one expert holding every token in order
+// (sorted[r] = r, padding T up to a multiple of bm), routing weight 1, and
+// the fp32 output accumulator zeroed.
+__global__ void __launch_bounds__(256) identity_grouping_kernel(int T, int bm, long long capacity,
+                                                                int32_t* __restrict__ sorted,
+                                                                int32_t* __restrict__ offsets,
+                                                                float* __restrict__ weights,
+                                                                float4* __restrict__ zero_buf,
+                                                                long long zero4) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long r = i0; r < capacity; r += stride) sorted[r] = r < T ? (int32_t)r : T;
+  for (long long r = i0; r < T; r += stride) weights[r] = 1.0f;
+  for (long long r = i0; r < zero4; r += stride) zero_buf[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (i0 == 0) {
+    offsets[0] = 0;
+    offsets[1] = (T + bm - 1) / bm * bm;
+  }
 }
 
 }  // namespace
+
+cudaError_t launch_identity_grouping(int T, int block_m, long long capacity, int32_t* sorted,
+                                     int32_t* offsets, float* weights, float* zero_buf,
+                                     long long zero_count, int num_sms, cudaStream_t st) {
+  long long work = capacity > zero_count / 4 ? capacity : zero_count / 4;
+  long long blocks = (work + 255) / 256;
+  if (blocks > (long long)num_sms * 4) blocks = (long long)num_sms * 4;
+  if (blocks < 1) blocks = 1;
+  identity_grouping_kernel<<<(int)blocks, 256, 0, st>>>(T, block_m, capacity, sorted, offsets,
+                                                        weights,
+                                                        reinterpret_cast<float4*>(zero_buf),
+                                                        zero_count / 4);
+  return cudaGetLastError();
+}
 
 namespace {
 inline bool align_single_block(int T, int k) {
@@ -127,9 +156,8 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
     if ((e = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   multi)) != cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(align_scatter_kernel,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, multi)) !=
-        cudaSuccess)
+    if ((e = cudaFuncSetAttribute(align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  multi + kMaxExperts * 4)) != cudaSuccess)
       return e;
     attr_done[dev] = true;
   }
@@ -144,10 +172,8 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
   const size_t smem = align_smem_bytes(kAlignBlockTokens / 32, E, top_k);
   align_count_kernel<<<nblocks, kAlignBlockTokens, smem, st>>>(topk_ids, T, top_k, E, scratch,
                                                                err);
-  align_scan_kernel<<<1, 256, 0, st>>>(nblocks, T, top_k, E, block_m, capacity, scratch, sorted,
-                                       offsets, counts);
-  align_scatter_kernel<<<nblocks, kAlignBlockTokens, smem, st>>>(topk_ids, T, top_k, E, scratch,
-                                                                 sorted, err);
+  align_place_kernel<<<nblocks, kAlignBlockTokens, smem + (size_t)E * 4, st>>>(
+      topk_ids, T, top_k, E, block_m, capacity, nblocks, scratch, sorted, offsets, counts);
   return cudaGetLastError();
 }
 

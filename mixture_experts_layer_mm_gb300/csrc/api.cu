@@ -153,7 +153,8 @@ int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* rout
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
   return cuda_status(launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, topk_ids,
-                                  topk_w, nullptr, 0, nullptr, static_cast<cudaStream_t>(stream)));
+                                  topk_w, nullptr, 0, nullptr, s->sms,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 int64_t mm_align_capacity(int T, int top_k, int E, int block_m) {
@@ -259,7 +260,7 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
   const bool fused = route_fuses_align(T, top_k);
   if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, &fa,
-                   st) != cudaSuccess ||
+                   s->sms, st) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
   if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
@@ -308,6 +309,46 @@ int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w, const uint1
                    uint16_t* out, void* stream) {
   return mm_moe_forward_ex(hidden, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm,
                            out, nullptr, 0, stream);
+}
+
+int64_t mm_gated_mlp_workspace_size(int T, int H, int I) {
+  if (T < 0 || H <= 0 || I <= 0 || H % 64 != 0 || I % 64 != 0) return -1;
+  return (int64_t)forward_layout(T, H, 1, I, 1).total;
+}
+
+int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16_t* w_down, int T,
+                 int H, int I, uint16_t* out, void* stream) {
+  if (T < 0 || H <= 0 || I <= 0) return MM_ERR_INVALID_ARG;
+  if (H % 64 != 0 || I % 64 != 0 || (long long)T * H >= (1LL << 40)) return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;
+  if (!hidden || !w_gate_up || !w_down || !out) return MM_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
+    return MM_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(T, H, 1, I, 1);  // one expert, k = 1
+  if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  if ((rc = ensure_ws(s, L.total)) != MM_OK) return rc;
+  void* ws = s->ws;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* w = at<float>(ws, L.w);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  uint16_t* act = at<uint16_t>(ws, L.act);
+  float* acc = at<float>(ws, L.acc);
+  const long long nacc = (long long)T * H;
+  if (launch_identity_grouping(T, kForwardBlockM, L.capacity, sorted, offsets, w, acc, nacc, s->sms,
+                               st) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, true, w_gate_up, act, sorted, offsets, nullptr,
+                          T, 1, 1, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, 1, 1, H, I,
+                          L.capacity, s->sms, s->status, st) != cudaSuccess)
+    return MM_ERR_CUDA;
+  return cuda_status(launch_finalize(acc, out, nacc, s->sms, st));
 }
 
 int mm_poll_device_status(void* stream) {

@@ -22,12 +22,13 @@
 // rows of every stage), straight into the swizzled layout. hidden stays in L2,
 // and no permuted copy of the activations is ever written.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over a static tile
-// stride): warp 0 = weight (A) TMA producer, warps 6-9 = token (B) producer
-// (warp 6 alone for TMA), warp 1 = TMEM allocator + MMA issuer, warps 2-5 =
-// epilogue (each reads its 32-lane quarter of tensor memory).
-// Two accumulator buffers let the epilogue of one tile overlap the
-// main loop of the next.
+// Warp roles (448 threads, one CTA per SM, persistent over a static tile
+// stride): warp 0 = weight (A) TMA producer, warps 10-13 = token (B) producer
+// (warp 10 alone for TMA), warp 1 = TMEM allocator + MMA issuer, warps 2-9 =
+// epilogue: warps w and w+4 read the same 32-lane quarter of tensor memory
+// and take alternate 32-column chunks of the tile.
+// Two accumulator buffers (256x128 tiles) let the epilogue of one tile
+// overlap the main loop of the next.
 //
 // Epilogues: gate_up writes act = bf16(silu(g) * u) ("模型与权重加载",
 // GatedMLP: silu_and_mul of the merged gate_up projection, gate first);
@@ -44,8 +45,12 @@ namespace mm {
 namespace {
 
 constexpr int kGM = 128;  // weight rows per MMA
-constexpr int kGK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kGemmThreads = 320;  // 10 warps: producers 0 and 6-9, MMA 1, epilogue 2-5
+// 14 warps: 0 = weight producer, 1 = MMA issuer, 2-9 = epilogue (two warps per
+// tensor-memory lane quarter), 10-13 = token producers.
+constexpr int kEpiWarp0 = 2, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
+constexpr int kBWarp0 = kEpiWarp0 + kEpiWarps;  // 10
+constexpr int kGemmThreads = (kBWarp0 + 4) * 32;  // 448
+constexpr int kEpiTok = 16;  // tokens per down-epilogue transpose step
 
 struct GemmArgs {
   const int32_t* sorted;   // [capacity]
@@ -73,28 +78,34 @@ constexpr int kBLsuGather = 2;  // four warps of cp.async from hidden (many rows
 // and the token producer fill a stage independently (each arrives on its
 // full barrier), but both wait for the same stage to be freed, so loads are
 // issued in the order the MMA needs them.
-template <int MODE, int BN, int S>
+// KB = K per stage: 64 (rows of 128 B, 128-byte swizzle) or 32 (rows of 64 B,
+// 64-byte swizzle: twice as many stages of half the size in the same shared
+// memory, so more bytes stay in flight while one stage is being consumed).
+template <int MODE, int BN, int S, int NACC, int KB>
 struct GemmCfg {
-  static constexpr int kABytes = kGM * kGK * 2;        // one 128-row weight tile
-  static constexpr int kBBytes = BN * kGK * 2;
+  static_assert(KB == 64 || KB == 32, "K per stage");
+  static constexpr int kRowBytes = KB * 2;              // one swizzle row
+  static constexpr int kABytes = kGM * KB * 2;          // one 128-row weight tile
+  static constexpr int kBBytes = BN * KB * 2;
   static constexpr int kStageBytes = 2 * kABytes + kBBytes;
-  static constexpr uint32_t kTmemCols = 4 * BN;  // 2 buffers x (D0, D1) x BN columns
-  static constexpr int kEpiBytes = MODE == MM_GEMM_DOWN ? 4 * 32 * 33 * 4 : 0;  // transpose tiles
+  static constexpr uint32_t kTmemCols = NACC * 2 * BN;  // NACC buffers x (D0, D1) x BN columns
+  // down epilogue: one [kEpiTok tokens][32 + 1] fp32 transpose tile per warp
+  static constexpr int kEpiBytes = MODE == MM_GEMM_DOWN ? kEpiWarps * kEpiTok * 33 * 4 : 0;
   static constexpr int kEpiOffset = S * kStageBytes;
   static constexpr int kSmemBytes = kEpiOffset + kEpiBytes + 1024;
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
-  static_assert(BN % 32 == 0 && BN <= 256, "BN");
+  static_assert(BN % 64 == 0 && BN <= 256, "BN: whole 32-column chunks for both epilogue sides");
   static_assert(kSmemBytes <= 227 * 1024 - 4096, "shared memory");
 };
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
+// 16-byte copy global -> shared (L2 only), zero-filled when !valid, with an
+// L2 eviction-priority hint.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid,
+                                                 uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(valid ? 16 : 0), "l"(policy)
                : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -133,11 +144,11 @@ __device__ __forceinline__ void signal_abort(int* flag, unsigned* err) {
   atomicOr(err, kDevErrTimeout);
 }
 
-template <int MODE, int BN, int S>
+template <int MODE, int BN, int S, int NACC, int KB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmX, const GemmArgs a) {
-  using Cfg = GemmCfg<MODE, BN, S>;
+  using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * S + 5];
   __shared__ uint32_t tmem_base_s;
@@ -194,9 +205,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&full[s]), 1 + (a.b_mode == kBLsuGather ? 128 : 1));
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
-      mbar_init(smem_u32(&tempty[b]), 128);
+      mbar_init(smem_u32(&tempty[b]), kEpiThreads);
     }
     mbar_init(smem_u32(done), 1);
     abort_s = 0;
@@ -213,7 +224,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_s;
-  const int nk = a.K / kGK;
+  const int nk = a.K / KB;
 
   if (warp == 0) {
     // --------------------------------------------- weight (A) TMA producer ---
@@ -237,8 +248,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t st = smem_base + s * Cfg::kStageBytes;
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, 2 * Cfg::kABytes);
-          tma_load_2d(st, &tmW, fb, kb * kGK, wrow0, pol_w);
-          tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * kGK, wrow1, pol_w);
+          tma_load_2d(st, &tmW, fb, kb * KB, wrow0, pol_w);
+          tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * KB, wrow1, pol_w);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -247,28 +258,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kBWarp0) {
     // -------------------------------------------------- token (B) producer ---
     const uint64_t pol_x = l2_policy_evict_last();
     int s = 0;
     uint32_t ph = 0;
     if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBLsuGather) {
-      // Warps 6-9 copy the chunk's token rows from hidden with 16-byte
-      // cp.async into the 128-byte-swizzled layout the MMA reads (16-byte
-      // chunk c of row r at r*128 + ((c ^ (r % 8)) * 16)). Thread (w, l) moves
-      // chunk l % 8 of rows p*16 + w*4 + l/8, p = 0..7. Each thread's copies
-      // arrive on the stage's barrier by themselves when they land
-      // (cp.async.mbarrier.arrive.noinc, 128 arrivals per stage); the MMA
+      // Warps 10-13 copy the chunk's token rows from hidden with 16-byte
+      // cp.async into the swizzled layout the MMA reads (16-byte chunk c of
+      // row r at r*RB + ((c ^ sw(r)) * 16), RB = row bytes, sw(r) = r % 8 for
+      // the 128-byte swizzle and (r / 2) % 4 for the 64-byte one). Thread
+      // (w, l) moves chunk l % CPR of rows p*RPP + w*(32/CPR) + l/CPR. Each
+      // thread's copies arrive on the stage's barrier by themselves when they
+      // land (cp.async.mbarrier.arrive.noinc, 128 arrivals per stage); the MMA
       // thread then fences the generic-to-async proxy before reading.
-      const int w = warp - 6, c16 = lane & 7;
-      const uint16_t* src[8];
-      const uint16_t* nxt[8];
-      auto fetch_rows = [&](int tl, const uint16_t* (&rows)[8]) {
+      constexpr int kCPR = KB / 8;            // 16-byte chunks per row
+      constexpr int kRPP = 128 / kCPR;        // rows per pass of the 128 threads
+      constexpr int kPasses = BN / kRPP;
+      const int w = warp - kBWarp0, c16 = lane % kCPR;
+      const uint16_t* src[kPasses];
+      const uint16_t* nxt[kPasses];
+      auto fetch_rows = [&](int tl, const uint16_t* (&rows)[kPasses]) {
         int e, m, row0, nrows;
         if (tl < total_tiles) decode_tile<BN>(tl, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-          const int r = p * 16 + w * 4 + (lane >> 3);
+        for (int p = 0; p < kPasses; ++p) {
+          const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
           const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
           rows[p] = f < a.Tk ? a.hidden + (size_t)(f / a.top_k) * a.K + c16 * 8 : nullptr;
         }
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
         if (aborted(&abort_s)) break;
 #pragma unroll
-        for (int p = 0; p < 8; ++p) src[p] = nxt[p];
+        for (int p = 0; p < kPasses; ++p) src[p] = nxt[p];
         fetch_rows(tile + gridDim.x, nxt);
         for (int kb = 0; kb < nk; ++kb) {
           if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
@@ -289,11 +304,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
 #pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            const int r = p * 16 + w * 4 + (lane >> 3);
-            const uint32_t dst = st + r * 128 + ((c16 ^ (r & 7)) << 4);
-            cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * kGK : a.hidden,
-                             src[p] != nullptr);
+          for (int p = 0; p < kPasses; ++p) {
+            const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
+            const int sw = KB == 64 ? (r & 7) : ((r >> 1) & 3);
+            const uint32_t dst = st + r * Cfg::kRowBytes + ((c16 ^ sw) << 4);
+            cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * KB : a.hidden,
+                             src[p] != nullptr, pol_x);
           }
           cp_async_arrive_noinc(smem_u32(&full[s]));
           if (++s == S) {
@@ -303,8 +319,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
       cp_async_wait<0>();  // no copy of this thread is in flight when the CTA ends
-    } else if (warp != 6) {
-      // Warps 7-9 help only on the cp.async path.
+    } else if (warp != kBWarp0) {
+      // Warps 11-13 help only on the cp.async path.
     } else if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBTmaGather) {
       // Token rows are gathered straight from hidden: lane i loads rows
       // 4i..4i+3 of the chunk with one tile::gather4 per stage. The rows of the
@@ -328,7 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int e, m, row0, nrows;
         decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
         const int n_g4 = ((nrows + 15) & ~15) / 4;  // rows the MMA reads, 4 per gather
-        const uint32_t bytes = n_g4 * 4 * kGK * 2;
+        const uint32_t bytes = n_g4 * 4 * Cfg::kRowBytes;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
@@ -342,7 +358,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
           __syncwarp();
           if (lane < n_g4)
-            tma_gather4(st + lane * 4 * kGK * 2, &tmX, fb, kb * kGK, rows[0], rows[1], rows[2],
+            tma_gather4(st + lane * 4 * Cfg::kRowBytes, &tmX, fb, kb * KB, rows[0], rows[1], rows[2],
                         rows[3], pol_x);
           if (++s == S) {
             s = 0;
@@ -366,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, Cfg::kBBytes);
-          tma_load_2d(st, &tmX, fb, kb * kGK, row0, pol_x);
+          tma_load_2d(st, &tmX, fb, kb * KB, row0, pol_x);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -385,8 +401,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (aborted(&abort_s)) break;
         int e, m, row0, nrows;
         decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
-        const int b = it & 1;
-        const uint32_t use = static_cast<uint32_t>(it >> 1);
+        const int b = it % NACC;
+        const uint32_t use = static_cast<uint32_t>(it / NACC);
         if (!mbar_wait(smem_u32(&tempty[b]), (use & 1u) ^ 1u)) {
           signal_abort(&abort_s, a.err);
           break;
@@ -408,10 +424,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
           const uint32_t st = smem_base + s * Cfg::kStageBytes;
 #pragma unroll
-          for (int kk = 0; kk < kGK / 16; ++kk) {
-            const uint64_t da0 = sdesc_k128(st + kk * 32);
-            const uint64_t da1 = sdesc_k128(st + Cfg::kABytes + kk * 32);
-            const uint64_t db = sdesc_k128(st + 2 * Cfg::kABytes + kk * 32);
+          for (int kk = 0; kk < KB / 16; ++kk) {
+            const uint64_t da0 = sdesc_kmajor<Cfg::kRowBytes>(st + kk * 32);
+            const uint64_t da1 = sdesc_kmajor<Cfg::kRowBytes>(st + Cfg::kABytes + kk * 32);
+            const uint64_t db = sdesc_kmajor<Cfg::kRowBytes>(st + 2 * Cfg::kABytes + kk * 32);
             const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
             umma_bf16(d0, da0, db, idesc, acc);
             umma_bf16(d1, da1, db, idesc, acc);
@@ -430,30 +446,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait(smem_u32(done), 0)) signal_abort(&abort_s, a.err);
     }
   } else {
-    // ----------------------------------------------------- epilogue (2-5) ---
-    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    // ----------------------------------------------------- epilogue (2-9) ---
+    const int q = warp & 3;                         // tensor-memory lane quarter this warp may read
+    const int side = (warp - kEpiWarp0) >> 2;       // takes 32-column chunks side, side + 2, ...
+    constexpr int kCh = BN / 64;                    // chunks per side
     const int r_in = q * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       if (aborted(&abort_s)) break;
       int e, m, row0, nrows;
       decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
-      const int b = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1);
-      // Down mode: lane j holds the slot id and routing weight of columns
-      // j, j+32, ... of this tile. They are loaded before the wait below, so
+      const int b = it % NACC;
+      const uint32_t use = static_cast<uint32_t>(it / NACC);
+      // Down mode: lane j holds the slot id and routing weight of column j of
+      // each of this warp's chunks. They are loaded before the wait below, so
       // their latency hides behind the tile's main loop.
-      int f_t[BN / 32];
-      float w_t[BN / 32];
+      int f_t[kCh];
+      float w_t[kCh];
       if (MODE == MM_GEMM_DOWN) {
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          const int c = cc * 32 + lane;
-          f_t[cc] = c < nrows ? __ldg(a.sorted + row0 + c) : a.Tk;
+        for (int i = 0; i < kCh; ++i) {
+          const int c = (2 * i + side) * 32 + lane;
+          f_t[i] = c < nrows ? __ldg(a.sorted + row0 + c) : a.Tk;
         }
 #pragma unroll
-        for (int cc = 0; cc < BN / 32; ++cc)
-          w_t[cc] = f_t[cc] < a.Tk ? __ldg(a.topk_w + f_t[cc]) : 0.f;
+        for (int i = 0; i < kCh; ++i) w_t[i] = f_t[i] < a.Tk ? __ldg(a.topk_w + f_t[i]) : 0.f;
       }
       if (!mbar_wait(smem_u32(&tfull[b]), use & 1u)) {
         signal_abort(&abort_s, a.err);
@@ -463,8 +480,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t tb =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * 2 * BN);
 #pragma unroll
-      for (int cc = 0; cc < BN / 32; ++cc) {
-        const int c0 = cc * 32;
+      for (int i = 0; i < kCh; ++i) {
+        const int c0 = (2 * i + side) * 32;
         if (c0 >= nrows) break;
         uint32_t g[32], u[32];
         tmem_ld_32x32b_x32(tb + c0, g);
@@ -472,49 +489,58 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tmem_wait_ld();
         const int ncol = min(32, nrows - c0);
         if (MODE == MM_GEMM_GATE_UP) {
-          const int i = m * kGM + r_in;  // intermediate index
-          if (i < a.N) {
-            uint16_t* dst = static_cast<uint16_t*>(a.C) + (size_t)(row0 + c0) * a.N + i;
+          const int i_out = m * kGM + r_in;  // intermediate index
+          if (i_out < a.N) {
+            uint16_t* dst = static_cast<uint16_t*>(a.C) + (size_t)(row0 + c0) * a.N + i_out;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               if (j < ncol) {
                 const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-                dst[(size_t)j * a.N] = f32_to_bf16_bits(gv / (1.0f + __expf(-gv)) * uv);
+                // silu(g) * u. The fast divide (about 2 ulp) is far below the
+                // bf16 rounding of the result; for g < -87.3, where 1 + e^-g
+                // exceeds 2^126, it returns 0 for a |silu(g)| under 1.1e-36.
+                dst[(size_t)j * a.N] =
+                    f32_to_bf16_bits(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
               }
             }
           }
         } else {
           // Column j's slot id and routing weight come from lane j by
-          // shuffle. The weighted 32x32 block of each
-          // accumulator goes through this warp's shared tile (row = token) so
-          // that each lane adds 4 consecutive outputs of one token with one
-          // 16-byte vector atomic.
-          const int f_l = f_t[cc];
-          const float w_l = w_t[cc];
+          // shuffle. The weighted values pass through this warp's shared
+          // tile (row = token), kEpiTok tokens at a time, so that each lane
+          // adds 4 consecutive outputs of one token with one 16-byte vector
+          // atomic.
+          const int f_l = f_t[i];
+          const float w_l = w_t[i];
           const int t_l = f_l / a.top_k;
           float* accp = static_cast<float*>(a.C);
           const uint64_t pol_acc = l2_policy_evict_last();  // keep the accumulator in L2
-          float* tr = epi_tile + (warp - 2) * 32 * 33;  // [token 32][h 32 + 1 pad]
-          const int hq = m * 2 * kGM + q * 32;            // first h of this warp's rows
+          float* tr = epi_tile + (warp - kEpiWarp0) * kEpiTok * 33;  // [kEpiTok][32 + 1 pad]
+          const int hq = m * 2 * kGM + q * 32;  // first h of this warp's rows
+          const int h4 = (lane & 7) * 4;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int hb = hq + half * kGM;
-            __syncwarp();
+          for (int part = 0; part < 2; ++part) {
+            const int hb = hq + part * kGM;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float wt = __shfl_sync(0xffffffffu, w_l, j);
-              tr[j * 33 + lane] = wt * __uint_as_float(half == 0 ? g[j] : u[j]);
-            }
-            __syncwarp();
-            const int h4 = (lane & 7) * 4;
+            for (int grp = 0; grp < 32 / kEpiTok; ++grp) {
+              __syncwarp();
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int jt = it * 4 + (lane >> 3);
-              const int f = __shfl_sync(0xffffffffu, f_l, jt);
-              const int t = __shfl_sync(0xffffffffu, t_l, jt);
-              if (jt < ncol && f < a.Tk && hb + h4 < a.N) {
-                const float* v = tr + jt * 33 + h4;
-                red_add_v4_f32(accp + (size_t)t * a.N + hb + h4, v[0], v[1], v[2], v[3], pol_acc);
+              for (int j = 0; j < kEpiTok; ++j) {
+                const int jj = grp * kEpiTok + j;
+                const float wt = __shfl_sync(0xffffffffu, w_l, jj);
+                tr[j * 33 + lane] = wt * __uint_as_float(part == 0 ? g[jj] : u[jj]);
+              }
+              __syncwarp();
+#pragma unroll
+              for (int s4 = 0; s4 < kEpiTok / 4; ++s4) {
+                const int jl = s4 * 4 + (lane >> 3);  // token within the group
+                const int jt = grp * kEpiTok + jl;
+                const int f = __shfl_sync(0xffffffffu, f_l, jt);
+                const int t = __shfl_sync(0xffffffffu, t_l, jt);
+                if (jt < ncol && f < a.Tk && hb + h4 < a.N) {
+                  const float* v = tr + jl * 33 + h4;
+                  red_add_v4_f32(accp + (size_t)t * a.N + hb + h4, v[0], v[1], v[2], v[3], pol_acc);
+                }
               }
             }
           }
@@ -556,29 +582,31 @@ EncodeTiledFn encode_fn() {
 
 // Row-major bf16 matrix [rows, cols] read in boxes of 64 columns x box_rows
 // rows with the 128-byte swizzle (the layout the MMA descriptors expect).
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              int kb) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kb), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            kb == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BN, int S>
+template <int MODE, int BN, int S, int NACC, int KB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
                        int top_k, int E, int N, int K, long long capacity, int num_sms,
                        unsigned* err, cudaStream_t st) {
-  using Cfg = GemmCfg<MODE, BN, S>;
+  using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, S>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, S, NACC, KB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -615,17 +643,19 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
     a.n_mtiles = (N + 2 * kGM - 1) / (2 * kGM);
   }
   CUtensorMap tmW, tmX;
-  if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM)) return cudaErrorInvalidValue;
+  if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM, KB)) return cudaErrorInvalidValue;
   // Gathered rows: X = hidden [T, K], one row per box; otherwise X holds the
   // token rows in segment order [capacity, K].
   // gather4 reads hidden [T, K] one row per box row; 2-D boxes read rows in
   // segment order [capacity, K]; the cp.async path does not use the map.
-  const bool ok_x = a.b_mode == kBTma ? make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN)
-                                      : make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1);
+  const bool ok_x = a.b_mode == kBTma
+                        ? make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN, KB)
+                        : make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1, KB);
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  grouped_gemm_kernel<MODE, BN, S><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX, a);
+  grouped_gemm_kernel<MODE, BN, S, NACC, KB><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX,
+                                                                                        a);
   return cudaGetLastError();
 }
 
@@ -651,11 +681,17 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
+  // 256x128 tiles with two accumulator sets: the epilogue of one tile overlaps
+  // the main loop of the next. (256x256 tiles with one set measured slower at
+  // every batch size: the epilogue no longer overlaps, and a segment just over
+  // 256 rows adds a nearly empty chunk that re-reads the whole weight tile.)
+  // (Stages of K = 32 with the 64-byte swizzle, 9 or 8 of them in the same
+  // shared memory, measured slower than 4 stages of K = 64 at every size.)
   if (mode == MM_GEMM_GATE_UP)
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 4>(X, x_is_hidden, W, C, sorted, offsets, topk_w, T,
-                                               top_k, E, N, K, capacity, num_sms, err, st);
-  return launch_cfg<MM_GEMM_DOWN, 128, 4>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E, N,
-                                          K, capacity, num_sms, err, st);
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets, topk_w,
+                                                  T, top_k, E, N, K, capacity, num_sms, err, st);
+  return launch_cfg<MM_GEMM_DOWN, 128, 4, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E,
+                                             N, K, capacity, num_sms, err, st);
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

@@ -182,18 +182,21 @@ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor for a K-major tile stored with the 128-byte
-// swizzle (rows of 64 bf16 = 128 B, 8-row atoms of 1024 B): start address at
-// bits 0-13, stride between 8-row groups (1024 B) at 32-45, descriptor
-// version 1 at 46, swizzle mode 2 (128 B) at 61-63. The leading-byte offset
-// is not used by swizzled K-major layouts.
-__device__ __forceinline__ uint64_t sdesc_k128(uint32_t smem_addr) {
+// Shared-memory matrix descriptor for a K-major tile stored with the SW-byte
+// swizzle (SW = 128: rows of 64 bf16, 8-row atoms of 1024 B; SW = 64: rows of
+// 32 bf16, 8-row atoms of 512 B): start address at bits 0-13, stride between
+// 8-row groups (8 * SW bytes) at 32-45, descriptor version 1 at 46, swizzle
+// mode at 61-63 (2 = 128 B, 4 = 64 B). The leading-byte offset is not used by
+// swizzled K-major layouts.
+template <int SW>
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t smem_addr) {
+  static_assert(SW == 128 || SW == 64, "swizzle span");
   uint64_t d = 0;
   d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>((8 * SW) >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(SW == 128 ? 2 : 4) << 61;
   return d;
 }
 

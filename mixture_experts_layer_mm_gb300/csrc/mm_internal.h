@@ -47,11 +47,11 @@ bool route_fuses_align(int T, int top_k);
 // Router logits + softmax + top-k (+ renorm). If zero_buf is non-null the same
 // launch also zeroes zero_count floats there (zero_count % 4 == 0). If
 // fuse_align is non-null and route_fuses_align(T, top_k), the launch also
-// produces the grouping.
+// produces the grouping. num_sms sizes the cluster split of H.
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
-                         const AlignOut* fuse_align, cudaStream_t st);
+                         const AlignOut* fuse_align, int num_sms, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);
@@ -59,6 +59,12 @@ long long align_scratch_ints(int T, int E, int top_k);
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, cudaStream_t st);
+
+// Grouping of a dense MLP (one expert, every token, weight 1) + zeroed
+// accumulator of zero_count floats.
+cudaError_t launch_identity_grouping(int T, int block_m, long long capacity, int32_t* sorted,
+                                     int32_t* offsets, float* weights, float* zero_buf,
+                                     long long zero_count, int num_sms, cudaStream_t st);
 
 // Whether the gate_up GEMM gathers token rows with TMA tile::gather4 (few rows
 // per expert) rather than with cp.async loader warps.

@@ -104,14 +104,6 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
   const int t0 = (blockIdx.x / ks) * kRtTok;
   const int hs = H / ks, hbase = (int)rank * hs;
 
-  if (zero_buf != nullptr) {  // fused zeroing of the fp32 output accumulator
-    float4* z = reinterpret_cast<float4*>(zero_buf);
-    const long long n4 = zero_count >> 2;
-    for (long long i = (long long)blockIdx.x * kRtThreads + tid; i < n4;
-         i += (long long)gridDim.x * kRtThreads)
-      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
   const int nk = hs / kRtKc;
   auto load_chunk = [&](int c) {
     if (c < nk) {
@@ -138,6 +130,15 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
 
 #pragma unroll
   for (int c = 0; c < kRtBufs; ++c) load_chunk(c);
+  // Fused zeroing of the fp32 output accumulator, issued after this CTA's
+  // first loads so that those do not queue behind the stores.
+  if (zero_buf != nullptr) {
+    float4* z = reinterpret_cast<float4*>(zero_buf);
+    const long long n4 = zero_count >> 2;
+    for (long long i = (long long)blockIdx.x * kRtThreads + tid; i < n4;
+         i += (long long)gridDim.x * kRtThreads)
+      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int c = 0; c < nk; ++c) {
     cp_async_wait<kRtBufs - 1>();
     __syncthreads();
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
 template <int EP>
 cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                       int H, int E, int top_k, int renorm, int32_t* ids, float* w, float* zero_buf,
-                      long long zero_count, const AlignOut& fa, cudaStream_t st) {
+                      long long zero_count, const AlignOut& fa, int num_sms, cudaStream_t st) {
   const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
   const size_t recv_bytes = (size_t)kRtTok * EP * sizeof(float);
   const size_t smem = gemm_bytes > recv_bytes ? gemm_bytes : recv_bytes;
@@ -313,14 +314,18 @@ cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const fl
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  // Cluster size: the largest of 8, 4, 2 that splits H into 64-wide chunks.
+  // Cluster size: the largest of 8, 4, 2 that splits H into 64-wide chunks
+  // and keeps the whole grid resident at once (CTAs per SM bounded by shared
+  // memory). Small batches get the widest split, which shortens each CTA's
+  // serial chain of loads; large batches have enough tiles without it.
+  const int tiles = (T + kRtTok - 1) / kRtTok;
+  const long long resident = (long long)num_sms * (int)((227 * 1024) / (smem + 1024));
   int ks = 1;
   for (int c = 8; c > 1; c >>= 1)
-    if (H % (kRtKc * c) == 0) {
+    if (H % (kRtKc * c) == 0 && (long long)tiles * c <= resident) {
       ks = c;
       break;
     }
-  const int tiles = (T + kRtTok - 1) / kRtTok;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * ks, 1, 1);
   cfg.blockDim = dim3(kRtThreads, 1, 1);
@@ -344,20 +349,20 @@ bool route_fuses_align(int T, int top_k) { return T <= kRtTok && T * top_k <= kA
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
-                         const AlignOut* fuse_align, cudaStream_t st) {
+                         const AlignOut* fuse_align, int num_sms, cudaStream_t st) {
   AlignOut fa = {};
   if (fuse_align != nullptr && route_fuses_align(T, top_k)) fa = *fuse_align;
   if (E <= 32)
     return launch_ep<32>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, fa, st);
+                         zero_buf, zero_count, fa, num_sms, st);
   if (E <= 64)
     return launch_ep<64>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, fa, st);
+                         zero_buf, zero_count, fa, num_sms, st);
   if (E <= 128)
     return launch_ep<128>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, fa, st);
+                          zero_buf, zero_count, fa, num_sms, st);
   return launch_ep<256>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w, zero_buf,
-                        zero_count, fa, st);
+                        zero_count, fa, num_sms, st);
 }
 
 }  // namespace mm

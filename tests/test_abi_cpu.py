@@ -88,6 +88,15 @@ def test_host_checks_before_any_cuda_call(lib):
         mm.MM_ERR_INVALID_ARG
 
 
+def test_gated_mlp_host_checks(lib):
+    L = mm.lib()
+    assert L.mm_gated_mlp(None, None, None, 4, 64, 64, None, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_gated_mlp(16, 16, 16, 4, 96, 64, 16, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_gated_mlp(16, 16, 16, -1, 64, 64, 16, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_gated_mlp(None, None, None, 0, 64, 64, None, None) == mm.MM_OK
+    assert mm.mm_gated_mlp_workspace_size(8, 128, 64) > 0
+
+
 def test_binding_raises_without_library(monkeypatch, tmp_path):
     import mixture_experts_layer_mm_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)
