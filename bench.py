@@ -404,7 +404,9 @@ def main():
                      "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
     fused_align = shape.T <= 64 and shape.T * k <= 8192
     single_align = shape.T <= 1024 and shape.T * k <= 8192
-    launches_per_step = 4 + (0 if fused_align else 1 if single_align else 2)
+    rows_gathered = shape.T * k > 64 * shape.E  # token rows copied into segment order
+    launches_per_step = (4 + (0 if fused_align else 1 if single_align else 2)
+                         + (1 if rows_gathered else 0))
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,

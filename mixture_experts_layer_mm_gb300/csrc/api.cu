@@ -81,11 +81,15 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t ids, w, sorted, offsets, counts, scratch, act, acc, total;
+  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
   long long capacity;
+  bool rows_in_order;  // token rows are copied into segment order before gate_up
 };
 
-ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
+// gather_rows: whether a gate_up with many rows per expert reads a copy of
+// the token rows in segment order (the MoE layer); a dense MLP's rows are in
+// order already.
+ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows = true) {
   ForwardLayout L;
   L.capacity = (long long)T * k + (long long)E * (kForwardBlockM - 1);
   size_t off = 0;
@@ -100,6 +104,10 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k) {
   L.offsets = take((size_t)(E + 1) * 4);
   L.counts = take((size_t)E * 4);
   L.scratch = take((size_t)align_scratch_ints(T, E, k) * 4);
+  // Many rows per expert: gate_up reads its token rows as 2-D TMA boxes of a
+  // copy in segment order (faster than gathering them inside the GEMM).
+  L.rows_in_order = gather_rows && !gate_up_gathers_rows(T, k, E);
+  L.xs = take(L.rows_in_order ? (size_t)L.capacity * H * 2 : 0);
   L.act = take((size_t)L.capacity * I * 2);
   L.acc = take((size_t)T * H * 4);
   L.total = off;
@@ -203,7 +211,7 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   return cuda_status(launch_grouped_gemm(mode, static_cast<const uint16_t*>(A),
                                          mode == MM_GEMM_GATE_UP, B, C, sorted_token_ids,
                                          expert_offsets, topk_w, T, top_k, E, N, K, capacity,
-                                         s->sms, s->status, st));
+                                         capacity, s->sms, s->status, st));
 }
 
 int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
@@ -266,13 +274,18 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
                              scratch, s->status, st) != cudaSuccess)
     return MM_ERR_CUDA;
+  uint16_t* xs = at<uint16_t>(ws, L.xs);
+  if (L.rows_in_order &&
+      launch_gather_rows(hidden, sorted, offsets, T, top_k, E, H, xs, s->sms, st) != cudaSuccess)
+    return MM_ERR_CUDA;
   if (!mark(2)) return MM_ERR_CUDA;
-  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, true, w_gate_up, act, sorted, offsets, nullptr,
-                          T, top_k, E, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, L.rows_in_order ? xs : hidden, !L.rows_in_order,
+                          w_gate_up, act, sorted, offsets, nullptr, T, top_k, E, I, H, L.capacity,
+                          L.capacity, s->sms, s->status, st) != cudaSuccess ||
       !mark(3))
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, top_k, E,
-                          H, I, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+                          H, I, L.capacity, L.capacity, s->sms, s->status, st) != cudaSuccess ||
       !mark(4))
     return MM_ERR_CUDA;
   if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(5)) return MM_ERR_CUDA;
@@ -313,7 +326,7 @@ int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w, const uint1
 
 int64_t mm_gated_mlp_workspace_size(int T, int H, int I) {
   if (T < 0 || H <= 0 || I <= 0 || H % 64 != 0 || I % 64 != 0) return -1;
-  return (int64_t)forward_layout(T, H, 1, I, 1).total;
+  return (int64_t)forward_layout(T, H, 1, I, 1, false).total;
 }
 
 int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16_t* w_down, int T,
@@ -324,7 +337,7 @@ int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16
   if (!hidden || !w_gate_up || !w_down || !out) return MM_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(w_gate_up) || !aligned16(w_down) || !aligned16(out))
     return MM_ERR_INVALID_ARG;
-  const ForwardLayout L = forward_layout(T, H, 1, I, 1);  // one expert, k = 1
+  const ForwardLayout L = forward_layout(T, H, 1, I, 1, false);  // one expert, k = 1
   if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   DevState* s = nullptr;
@@ -342,11 +355,13 @@ int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16
   if (launch_identity_grouping(T, kForwardBlockM, L.capacity, sorted, offsets, w, acc, nacc, s->sms,
                                st) != cudaSuccess)
     return MM_ERR_CUDA;
-  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, true, w_gate_up, act, sorted, offsets, nullptr,
-                          T, 1, 1, I, H, L.capacity, s->sms, s->status, st) != cudaSuccess)
+  // The rows are in order already: gate_up reads hidden by 2-D TMA boxes
+  // (rows past T read as zeros).
+  if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, false, w_gate_up, act, sorted, offsets, nullptr,
+                          T, 1, 1, I, H, L.capacity, T, s->sms, s->status, st) != cudaSuccess)
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, 1, 1, H, I,
-                          L.capacity, s->sms, s->status, st) != cudaSuccess)
+                          L.capacity, L.capacity, s->sms, s->status, st) != cudaSuccess)
     return MM_ERR_CUDA;
   return cuda_status(launch_finalize(acc, out, nacc, s->sms, st));
 }

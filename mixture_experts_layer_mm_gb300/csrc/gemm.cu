@@ -600,8 +600,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 template <int MODE, int BN, int S, int NACC, int KB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
-                       int top_k, int E, int N, int K, long long capacity, int num_sms,
-                       unsigned* err, cudaStream_t st) {
+                       int top_k, int E, int N, int K, long long capacity, long long x_rows,
+                       int num_sms, unsigned* err, cudaStream_t st) {
   using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -649,7 +649,7 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   // gather4 reads hidden [T, K] one row per box row; 2-D boxes read rows in
   // segment order [capacity, K]; the cp.async path does not use the map.
   const bool ok_x = a.b_mode == kBTma
-                        ? make_map(&tmX, X, (uint64_t)capacity, (uint64_t)K, BN, KB)
+                        ? make_map(&tmX, X, (uint64_t)x_rows, (uint64_t)K, BN, KB)
                         : make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1, KB);
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
@@ -657,6 +657,27 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   grouped_gemm_kernel<MODE, BN, S, NACC, KB><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX,
                                                                                         a);
   return cudaGetLastError();
+}
+
+// Token rows in segment order: xs[r] = hidden[sorted[r] / k] for the rows of
+// the expert segments (r < offsets[E]); padding rows become zeros. One warp
+// per row, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ hidden,
+                                                          const int32_t* __restrict__ sorted,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int top_k, int Tk, int row16,
+                                                          uint4* __restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const int rows = __ldg(offsets + E);
+  const int wstride = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += wstride) {
+    const int f = __ldg(sorted + r);
+    const uint4* src = f < Tk ? hidden + (size_t)(f / top_k) * row16 : nullptr;
+    uint4* dst = xs + (size_t)r * row16;
+#pragma unroll 4
+    for (int i = lane; i < row16; i += 32)
+      dst[i] = src != nullptr ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
@@ -680,7 +701,8 @@ bool gate_up_gathers_rows(int T, int top_k, int E) {
 cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
-                                long long capacity, int num_sms, unsigned* err, cudaStream_t st) {
+                                long long capacity, long long x_rows, int num_sms, unsigned* err,
+                                cudaStream_t st) {
   // 256x128 tiles with two accumulator sets: the epilogue of one tile overlaps
   // the main loop of the next. (256x256 tiles with one set measured slower at
   // every batch size: the epilogue no longer overlaps, and a segment just over
@@ -688,10 +710,20 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
   // (Stages of K = 32 with the 64-byte swizzle, 9 or 8 of them in the same
   // shared memory, measured slower than 4 stages of K = 64 at every size.)
   if (mode == MM_GEMM_GATE_UP)
-    return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets, topk_w,
-                                                  T, top_k, E, N, K, capacity, num_sms, err, st);
-  return launch_cfg<MM_GEMM_DOWN, 128, 4, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T, top_k, E,
-                                             N, K, capacity, num_sms, err, st);
+    return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,
+                                                      topk_w, T, top_k, E, N, K, capacity, x_rows,
+                                                      num_sms, err, st);
+  return launch_cfg<MM_GEMM_DOWN, 128, 4, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T, top_k,
+                                                 E, N, K, capacity, x_rows, num_sms, err, st);
+}
+
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
+                               const int32_t* offsets, int T, int top_k, int E, int H,
+                               uint16_t* xs, int num_sms, cudaStream_t st) {
+  gather_rows_kernel<<<num_sms * 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), sorted,
+                                                  offsets, E, top_k, T * top_k, H / 8,
+                                                  reinterpret_cast<uint4*>(xs));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,

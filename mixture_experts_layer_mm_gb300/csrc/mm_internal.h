@@ -72,15 +72,22 @@ bool gate_up_gathers_rows(int T, int top_k, int E);
 
 // Grouped GEMM on tcgen05. mode 0: C = act bf16 [capacity, N] = silu(gate) *
 // up; X = hidden [T, K] with rows gathered through sorted / top_k when
-// x_is_hidden (always, from the library's entry points), else X = token rows
-// already in segment order [capacity, K].
-// mode 1: X = act [capacity, K], C = fp32 acc [T, N] += topk_w * (X W^T).
+// x_is_hidden, else X = token rows already in segment order [x_rows, K]
+// (rows at or past x_rows read as zeros).
+// mode 1: X = act [x_rows, K], C = fp32 acc [T, N] += topk_w * (X W^T).
 cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
-                                long long capacity, int num_sms, unsigned* err, cudaStream_t st);
+                                long long capacity, long long x_rows, int num_sms, unsigned* err,
+                                cudaStream_t st);
 
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
+// xs[r] = hidden[sorted[r] / top_k] (H bf16 per row) for r < offsets[E];
+// padding rows of the segments become zeros. H % 8 == 0.
+cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
+                               const int32_t* offsets, int T, int top_k, int E, int H,
+                               uint16_t* xs, int num_sms, cudaStream_t st);
+
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
                             cudaStream_t st);
 
