@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(1024) align_single_kernel(
     int32_t* __restrict__ sorted, int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
     unsigned* err) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
   align_one_block(ids, T, k, E, bm, capacity, sorted, offsets, counts, err, smem);
 }
 
@@ -37,6 +39,8 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_count_kernel(
   constexpr int W = kAlignBlockTokens / 32;
   const AlignSmem S = carve(smem, W, E);
   const int tok0 = blockIdx.x * kAlignBlockTokens;
+  pdl_wait();
+  pdl_trigger();
   stage_ids(ids, T, k, tok0, S.ids);
   __syncthreads();
   block_ballots(S.ids, T, k, E, tok0, S.bal, err);
@@ -62,6 +66,8 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
   const AlignSmem S = carve(smem, W, E);
   int* base_s = reinterpret_cast<int*>(smem + align_smem_bytes(W, E, k));  // [E]
   const int tok0 = blockIdx.x * kAlignBlockTokens;
+  pdl_wait();
+  pdl_trigger();
   stage_ids(ids, T, k, tok0, S.ids);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int before = 0, total = 0;
@@ -104,6 +110,7 @@ __global__ void __launch_bounds__(256) identity_grouping_kernel(int T, int bm, l
                                                                 long long zero4) {
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long i0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_trigger();
   for (long long r = i0; r < capacity; r += stride) sorted[r] = r < T ? (int32_t)r : T;
   for (long long r = i0; r < T; r += stride) weights[r] = 1.0f;
   for (long long r = i0; r < zero4; r += stride) zero_buf[r] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -122,11 +129,9 @@ cudaError_t launch_identity_grouping(int T, int block_m, long long capacity, int
   long long blocks = (work + 255) / 256;
   if (blocks > (long long)num_sms * 4) blocks = (long long)num_sms * 4;
   if (blocks < 1) blocks = 1;
-  identity_grouping_kernel<<<(int)blocks, 256, 0, st>>>(T, block_m, capacity, sorted, offsets,
-                                                        weights,
-                                                        reinterpret_cast<float4*>(zero_buf),
-                                                        zero_count / 4);
-  return cudaGetLastError();
+  return launch_k(identity_grouping_kernel, dim3((int)blocks), dim3(256), 0, st, false, T,
+                  block_m, capacity, sorted, offsets, weights,
+                  reinterpret_cast<float4*>(zero_buf), zero_count / 4);
 }
 
 namespace {
@@ -142,7 +147,7 @@ long long align_scratch_ints(int T, int E, int k) {
 
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
-                         int32_t* scratch, unsigned* err, cudaStream_t st) {
+                         int32_t* scratch, unsigned* err, bool after_prev, cudaStream_t st) {
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
   if (!attr_done[dev]) {
@@ -164,17 +169,17 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
   if (align_single_block(T, top_k)) {
     const int nwarps = T <= 32 ? 1 : (T + 31) / 32;
     const size_t smem = align_smem_bytes(nwarps, E, top_k);
-    align_single_kernel<<<1, nwarps * 32, smem, st>>>(topk_ids, T, top_k, E, block_m, capacity,
-                                                      sorted, offsets, counts, err);
-    return cudaGetLastError();
+    return launch_k(align_single_kernel, dim3(1), dim3(nwarps * 32), smem, st, after_prev,
+                    topk_ids, T, top_k, E, block_m, capacity, sorted, offsets, counts, err);
   }
   const int nblocks = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
   const size_t smem = align_smem_bytes(kAlignBlockTokens / 32, E, top_k);
-  align_count_kernel<<<nblocks, kAlignBlockTokens, smem, st>>>(topk_ids, T, top_k, E, scratch,
-                                                               err);
-  align_place_kernel<<<nblocks, kAlignBlockTokens, smem + (size_t)E * 4, st>>>(
-      topk_ids, T, top_k, E, block_m, capacity, nblocks, scratch, sorted, offsets, counts);
-  return cudaGetLastError();
+  cudaError_t e = launch_k(align_count_kernel, dim3(nblocks), dim3(kAlignBlockTokens), smem, st,
+                           after_prev, topk_ids, T, top_k, E, scratch, err);
+  if (e != cudaSuccess) return e;
+  return launch_k(align_place_kernel, dim3(nblocks), dim3(kAlignBlockTokens),
+                  smem + (size_t)E * 4, st, true, topk_ids, T, top_k, E, block_m, capacity,
+                  nblocks, static_cast<const int32_t*>(scratch), sorted, offsets, counts);
 }
 
 }  // namespace mm

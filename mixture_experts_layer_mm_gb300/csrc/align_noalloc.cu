@@ -58,11 +58,12 @@ extern "C" int mm_align_noalloc(const int32_t* topk_ids, int T, int top_k, int E
   if (rc != MM_OK) return rc;
   unsigned* status = nullptr;
   if ((rc = mm::current_status_word(&status)) != MM_OK) return rc;
-  // The count kernel writes every scratch entry the scan kernel reads, so the
-  // previous call's contents never need clearing.
+  // The count kernel writes every scratch entry the place kernel reads, so
+  // the previous call's contents never need clearing.
   const cudaError_t e = mm::launch_align(topk_ids, T, top_k, E, block_m,
                                          mm_align_capacity(T, top_k, E, block_m),
                                          sorted_token_ids, expert_offsets, expert_counts,
-                                         scratch, status, static_cast<cudaStream_t>(stream));
+                                         scratch, status, false,
+                                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MM_OK : MM_ERR_CUDA;
 }

@@ -161,7 +161,7 @@ int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* rout
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
   return cuda_status(launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, topk_ids,
-                                  topk_w, nullptr, 0, nullptr, s->sms,
+                                  topk_w, nullptr, 0, nullptr, s->sms, s->status,
                                   static_cast<cudaStream_t>(stream)));
 }
 
@@ -186,7 +186,7 @@ int mm_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
   return cuda_status(launch_align(topk_ids, T, top_k, E, block_m,
                                   mm_align_capacity(T, top_k, E, block_m), sorted_token_ids,
                                   expert_offsets, expert_counts, static_cast<int32_t*>(s->ws),
-                                  s->status, static_cast<cudaStream_t>(stream)));
+                                  s->status, false, static_cast<cudaStream_t>(stream)));
 }
 
 int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
@@ -211,7 +211,7 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
   return cuda_status(launch_grouped_gemm(mode, static_cast<const uint16_t*>(A),
                                          mode == MM_GEMM_GATE_UP, B, C, sorted_token_ids,
                                          expert_offsets, topk_w, T, top_k, E, N, K, capacity,
-                                         capacity, s->sms, s->status, st));
+                                         capacity, s->sms, s->status, false, st));
 }
 
 int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
@@ -268,27 +268,29 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
   const bool fused = route_fuses_align(T, top_k);
   if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, &fa,
-                   s->sms, st) != cudaSuccess ||
+                   s->sms, s->status, st) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
   if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
-                             scratch, s->status, st) != cudaSuccess)
+                             scratch, s->status, true, st) != cudaSuccess)
     return MM_ERR_CUDA;
   uint16_t* xs = at<uint16_t>(ws, L.xs);
   if (L.rows_in_order &&
-      launch_gather_rows(hidden, sorted, offsets, T, top_k, E, H, xs, s->sms, st) != cudaSuccess)
+      launch_gather_rows(hidden, sorted, offsets, T, top_k, E, H, xs, s->sms, true, st) !=
+          cudaSuccess)
     return MM_ERR_CUDA;
   if (!mark(2)) return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_GATE_UP, L.rows_in_order ? xs : hidden, !L.rows_in_order,
                           w_gate_up, act, sorted, offsets, nullptr, T, top_k, E, I, H, L.capacity,
-                          L.capacity, s->sms, s->status, st) != cudaSuccess ||
+                          L.capacity, s->sms, s->status, true, st) != cudaSuccess ||
       !mark(3))
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, top_k, E,
-                          H, I, L.capacity, L.capacity, s->sms, s->status, st) != cudaSuccess ||
+                          H, I, L.capacity, L.capacity, s->sms, s->status, true, st) != cudaSuccess ||
       !mark(4))
     return MM_ERR_CUDA;
-  if (launch_finalize(acc, out, nacc, s->sms, st) != cudaSuccess || !mark(5)) return MM_ERR_CUDA;
+  if (launch_finalize(acc, out, nacc, s->sms, true, st) != cudaSuccess || !mark(5))
+    return MM_ERR_CUDA;
   return MM_OK;
 }
 
@@ -358,12 +360,12 @@ int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16
   // The rows are in order already: gate_up reads hidden by 2-D TMA boxes
   // (rows past T read as zeros).
   if (launch_grouped_gemm(MM_GEMM_GATE_UP, hidden, false, w_gate_up, act, sorted, offsets, nullptr,
-                          T, 1, 1, I, H, L.capacity, T, s->sms, s->status, st) != cudaSuccess)
+                          T, 1, 1, I, H, L.capacity, T, s->sms, s->status, true, st) != cudaSuccess)
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, 1, 1, H, I,
-                          L.capacity, L.capacity, s->sms, s->status, st) != cudaSuccess)
+                          L.capacity, L.capacity, s->sms, s->status, true, st) != cudaSuccess)
     return MM_ERR_CUDA;
-  return cuda_status(launch_finalize(acc, out, nacc, s->sms, st));
+  return cuda_status(launch_finalize(acc, out, nacc, s->sms, true, st));
 }
 
 int mm_poll_device_status(void* stream) {

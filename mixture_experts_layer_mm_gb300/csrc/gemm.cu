@@ -158,6 +158,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E;
+  pdl_wait();  // the grouping and the token rows come from the kernels before
+  pdl_trigger();
 
   // Chunk table: cs_s[e] = index of expert e's first token chunk.
   for (int i = tid; i <= E; i += kGemmThreads) off_s[i] = a.offsets[i];
@@ -580,10 +582,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] read in boxes of 64 columns x box_rows
-// rows with the 128-byte swizzle (the layout the MMA descriptors expect).
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              int kb) {
+// Row-major bf16 matrix [rows, cols] read in boxes of kb columns x box_rows
+// rows with the 2*kb-byte swizzle (the layout the MMA descriptors expect).
+}  // namespace
+
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, int kb) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -597,11 +601,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
 template <int MODE, int BN, int S, int NACC, int KB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
                        int top_k, int E, int N, int K, long long capacity, long long x_rows,
-                       int num_sms, unsigned* err, cudaStream_t st) {
+                       int num_sms, unsigned* err, bool after_prev, cudaStream_t st) {
   using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -643,20 +648,20 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
     a.n_mtiles = (N + 2 * kGM - 1) / (2 * kGM);
   }
   CUtensorMap tmW, tmX;
-  if (!make_map(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM, KB)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_2d(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM, KB))
+    return cudaErrorInvalidValue;
   // Gathered rows: X = hidden [T, K], one row per box; otherwise X holds the
   // token rows in segment order [capacity, K].
   // gather4 reads hidden [T, K] one row per box row; 2-D boxes read rows in
   // segment order [capacity, K]; the cp.async path does not use the map.
   const bool ok_x = a.b_mode == kBTma
-                        ? make_map(&tmX, X, (uint64_t)x_rows, (uint64_t)K, BN, KB)
-                        : make_map(&tmX, X, (uint64_t)T, (uint64_t)K, 1, KB);
+                        ? make_tensor_map_2d(&tmX, X, (uint64_t)x_rows, (uint64_t)K, BN, KB)
+                        : make_tensor_map_2d(&tmX, X, (uint64_t)T, (uint64_t)K, 1, KB);
   if (!ok_x) return cudaErrorInvalidValue;
   const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  grouped_gemm_kernel<MODE, BN, S, NACC, KB><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmW, tmX,
-                                                                                        a);
-  return cudaGetLastError();
+  return launch_k(grouped_gemm_kernel<MODE, BN, S, NACC, KB>, dim3(grid), dim3(kGemmThreads),
+                  Cfg::kSmemBytes, st, after_prev, tmW, tmX, a);
 }
 
 // Token rows in segment order: xs[r] = hidden[sorted[r] / k] for the rows of
@@ -668,6 +673,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           int E, int top_k, int Tk, int row16,
                                                           uint4* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
   const int rows = __ldg(offsets + E);
   const int wstride = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += wstride) {
@@ -682,6 +689,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
                                                        uint2* __restrict__ out, long long n4) {
+  pdl_wait();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 v = acc[i];
@@ -702,7 +710,7 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, long long x_rows, int num_sms, unsigned* err,
-                                cudaStream_t st) {
+                                bool after_prev, cudaStream_t st) {
   // 256x128 tiles with two accumulator sets: the epilogue of one tile overlaps
   // the main loop of the next. (256x256 tiles with one set measured slower at
   // every batch size: the epilogue no longer overlaps, and a segment just over
@@ -712,30 +720,29 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
   if (mode == MM_GEMM_GATE_UP)
     return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,
                                                       topk_w, T, top_k, E, N, K, capacity, x_rows,
-                                                      num_sms, err, st);
+                                                      num_sms, err, after_prev, st);
   return launch_cfg<MM_GEMM_DOWN, 128, 4, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T, top_k,
-                                                 E, N, K, capacity, x_rows, num_sms, err, st);
+                                                 E, N, K, capacity, x_rows, num_sms, err,
+                                                 after_prev, st);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
                                const int32_t* offsets, int T, int top_k, int E, int H,
-                               uint16_t* xs, int num_sms, cudaStream_t st) {
-  gather_rows_kernel<<<num_sms * 8, 256, 0, st>>>(reinterpret_cast<const uint4*>(hidden), sorted,
-                                                  offsets, E, top_k, T * top_k, H / 8,
-                                                  reinterpret_cast<uint4*>(xs));
-  return cudaGetLastError();
+                               uint16_t* xs, int num_sms, bool after_prev, cudaStream_t st) {
+  return launch_k(gather_rows_kernel, dim3(num_sms * 8), dim3(256), 0, st, after_prev,
+                  reinterpret_cast<const uint4*>(hidden), sorted, offsets, E, top_k, T * top_k,
+                  H / 8, reinterpret_cast<uint4*>(xs));
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
-                            cudaStream_t st) {
+                            bool after_prev, cudaStream_t st) {
   const long long n4 = n / 4;
   long long blocks = (n4 + 255) / 256;
   const long long cap_blocks = (long long)num_sms * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
   if (blocks < 1) blocks = 1;
-  finalize_kernel<<<(int)blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(acc),
-                                               reinterpret_cast<uint2*>(out), n4);
-  return cudaGetLastError();
+  return launch_k(finalize_kernel, dim3((int)blocks), dim3(256), 0, st, after_prev,
+                  reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(out), n4);
 }
 
 }  // namespace mm

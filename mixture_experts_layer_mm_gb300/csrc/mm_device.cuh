@@ -89,6 +89,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch. pdl_wait: wait until the kernel before this
+// one on the stream has completed and its memory operations are visible
+// (returns at once for a launch without programmatic serialisation).
+// pdl_trigger: the next kernel on the stream may be scheduled now.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2-D tiled bulk tensor load into shared memory; completion is signalled as
 // transaction bytes on mbarrier `bar`. c0 is the inner (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar,

@@ -2,11 +2,33 @@
 // is include/mm.h and is implemented in api.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace mm {
+
+// Launches kern<<<grid, block, smem, st>>>(args...). With after_prev the
+// launch uses programmatic stream serialisation: it may be scheduled while
+// the previous kernel of the layer finishes, and the kernel waits for it
+// (griddepcontrol.wait) in every CTA before it touches memory. Only kernels
+// that follow another kernel of the same layer call are launched this way.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, bool after_prev, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prev ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
@@ -47,24 +69,40 @@ bool route_fuses_align(int T, int top_k);
 // Router logits + softmax + top-k (+ renorm). If zero_buf is non-null the same
 // launch also zeroes zero_count floats there (zero_count % 4 == 0). If
 // fuse_align is non-null and route_fuses_align(T, top_k), the launch also
-// produces the grouping. num_sms sizes the cluster split of H.
+// produces the grouping. num_sms sizes the grid; err is the device status
+// word (bounded waits that run out set kDevErrTimeout there).
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
-                         const AlignOut* fuse_align, int num_sms, cudaStream_t st);
+                         const AlignOut* fuse_align, int num_sms, unsigned* err,
+                         cudaStream_t st);
+
+// Whether launch_route runs the tensor-core router (route_tc.cu) for this
+// batch, and that router's launcher (same arguments, no grouping).
+bool route_uses_tensor_cores(int T, int E);
+cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                            int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
+                            float* topk_w, float* zero_buf, long long zero_count, int num_sms,
+                            unsigned* err, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);
 
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
-                         int32_t* scratch, unsigned* err, cudaStream_t st);
+                         int32_t* scratch, unsigned* err, bool after_prev, cudaStream_t st);
 
 // Grouping of a dense MLP (one expert, every token, weight 1) + zeroed
 // accumulator of zero_count floats.
 cudaError_t launch_identity_grouping(int T, int block_m, long long capacity, int32_t* sorted,
                                      int32_t* offsets, float* weights, float* zero_buf,
                                      long long zero_count, int num_sms, cudaStream_t st);
+
+// Tensor map of a row-major bf16 matrix [rows, cols] read in boxes of kb
+// columns (64 or 32) x box_rows rows with the 2*kb-byte swizzle the MMA
+// descriptors expect; rows past `rows` read as zeros.
+bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, int kb);
 
 // Whether the gate_up GEMM gathers token rows with TMA tile::gather4 (few rows
 // per expert) rather than with cp.async loader warps.
@@ -79,16 +117,16 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, long long x_rows, int num_sms, unsigned* err,
-                                cudaStream_t st);
+                                bool after_prev, cudaStream_t st);
 
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
 // xs[r] = hidden[sorted[r] / top_k] (H bf16 per row) for r < offsets[E];
 // padding rows of the segments become zeros. H % 8 == 0.
 cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
                                const int32_t* offsets, int T, int top_k, int E, int H,
-                               uint16_t* xs, int num_sms, cudaStream_t st);
+                               uint16_t* xs, int num_sms, bool after_prev, cudaStream_t st);
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
-                            cudaStream_t st);
+                            bool after_prev, cudaStream_t st);
 
 }  // namespace mm

@@ -23,6 +23,7 @@
 #include "align_block.cuh"
 #include "mm_device.cuh"
 #include "mm_internal.h"
+#include "route_finish.cuh"
 
 namespace mm {
 namespace {
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
+  pdl_trigger();  // the next kernel of the layer may be scheduled (it waits for this one)
   const int t0 = (blockIdx.x / ks) * kRtTok;
   const int hs = H / ks, hbase = (int)rank * hs;
 
@@ -219,73 +221,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
         l[q] = v + (bias != nullptr ? bias[e] : 0.f);
       }
     }
-    float m = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) m = fmaxf(m, l[q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z[Q], s = 0.f;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-      z[q] = (lane + 32 * q < E) ? expf(l[q] - m) : 0.f;
-      s += z[q];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-
-    // k rounds of warp arg-max: the larger logit wins, equal logits go to the
-    // lower expert id. A logit is compared as an order-preserving uint32 key
-    // (exact: -0 is first folded into +0), so one warp-wide max reduction
-    // finds the best value and one min reduction picks the lowest id
-    // holding it.
-    uint32_t key[Q];
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-      const uint32_t b = __float_as_uint(l[q] + 0.0f);
-      key[q] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    }
-    uint32_t sel = 0;
-    for (int round = 0; round < top_k; ++round) {
-      uint32_t bk = 0;
-      int bq = Q;  // none
-#pragma unroll
-      for (int q = 0; q < Q; ++q)  // ascending ids: strict '>' keeps the lower id on ties
-        if (lane + 32 * q < E && !((sel >> q) & 1u) && (bq == Q || key[q] > bk)) {
-          bk = key[q];
-          bq = q;
-        }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, bq < Q ? bk : 0u);
-      const uint32_t cand = (bq < Q && bk == m) ? static_cast<uint32_t>(bq * 32 + lane) : 0xffffffffu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      if ((int)(win & 31u) == lane) sel |= 1u << (win >> 5);
-    }
-
-    // Probabilities of the selected experts, renormalised if asked.
-    float psel = 0.f;
-#pragma unroll
-    for (int q = 0; q < Q; ++q)
-      if ((sel >> q) & 1u) psel += z[q] / s;
-    float denom = 1.f;
-    if (renorm) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) psel += __shfl_xor_sync(0xffffffffu, psel, o);
-      denom = psel;
-    }
-    // Ascending expert order: slot = number of selected experts with a lower id.
-    int base = 0;
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-      const bool mine = (sel >> q) & 1u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, mine);
-      if (mine) {
-        const int slot = base + __popc(bal & lt);
-        const float p = z[q] / s;
-        ids_out[(size_t)t * top_k + slot] = lane + 32 * q;
-        w_out[(size_t)t * top_k + slot] = renorm ? p / denom : p;
-      }
-      base += __popc(bal);
-    }
+    routefin::finish_token<Q>(l, E, top_k, renorm, t, ids_out, w_out);
   }
   // The grouping (T <= 64) needs every CTA's ids: one more cluster barrier.
   if (fa.sorted != nullptr) {
@@ -349,7 +285,12 @@ bool route_fuses_align(int T, int top_k) { return T <= kRtTok && T * top_k <= kA
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
-                         const AlignOut* fuse_align, int num_sms, cudaStream_t st) {
+                         const AlignOut* fuse_align, int num_sms, unsigned* err,
+                         cudaStream_t st) {
+  // More than one 64-token tile and at most 128 experts: the tcgen05 router.
+  if (route_uses_tensor_cores(T, E))
+    return launch_route_tc(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
+                           zero_buf, zero_count, num_sms, err, st);
   AlignOut fa = {};
   if (fuse_align != nullptr && route_fuses_align(T, top_k)) fa = *fuse_align;
   if (E <= 32)

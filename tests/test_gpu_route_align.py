@@ -72,6 +72,34 @@ def test_route_shapes(T, H, E, k, renorm, bias):
     _check_route(d["hidden"], d["router_w"], d["router_bias"], k, renorm)
 
 
+# Batches above 4096 tokens take the tensor-core router: odd expert counts
+# (rows past E of its 128-row tile), bias, no renorm, k up to 32, and a ragged
+# last 128-token tile.
+@pytest.mark.parametrize("T,H,E,k,renorm,bias", [
+    (4097, 64, 33, 7, True, True), (4500, 128, 128, 8, False, False),
+    (5000, 192, 97, 32, True, False), (8192, 64, 64, 1, False, True),
+])
+def test_route_tensor_core_shapes(T, H, E, k, renorm, bias):
+    d = random_small_inputs(T + E + k, T, H, E, 64, bias=bias)
+    _check_route(d["hidden"], d["router_w"], d["router_bias"], k, renorm)
+
+
+def test_route_tensor_core_forced_ties():
+    # As below, at a batch size that takes the tensor-core router: exact ties
+    # between experts of both halves of each thread pair's split.
+    T, H, E, k = 4200, 64, 128, 8
+    c = (np.arange(E) % 5 + 1).astype(np.float64)  # values 1..5, each ~26 times
+    bias = np.log(c).astype(np.float32)
+    hidden = random_small_inputs(7, T, H, E, 64)["hidden"]
+    rw = np.zeros((E, H), dtype=np.uint16)
+    ids_g, w_g = mm.mm_route(dev_bf16(hidden), dev_bf16(rw), k, False, router_bias=f32_dev(bias))
+    ids_g = ids_g.cpu().numpy()
+    ids_ref, w_ref, _ = O.route(hidden, rw, k, False, bias)
+    assert np.array_equal(ids_g, ids_ref)
+    assert (ids_g == np.array([4, 9, 14, 19, 24, 29, 34, 39])[None, :]).all()
+    np.testing.assert_allclose(w_g.cpu().numpy(), w_ref, rtol=W_RTOL)
+
+
 def test_route_forced_ties():
     # Router weights zero, bias ln(c) with repeated c: exact ties resolved to
     # the lower expert id, identically on both sides.
