@@ -72,22 +72,26 @@ def test_route_shapes(T, H, E, k, renorm, bias):
     _check_route(d["hidden"], d["router_w"], d["router_bias"], k, renorm)
 
 
-# Batches above 4096 tokens take the tensor-core router: odd expert counts
-# (rows past E of its 128-row tile), bias, no renorm, k up to 32, and a ragged
-# last 128-token tile.
+# Batches above 2048 tokens with at most 128 experts take the tensor-core
+# router, with 32-, 64- or 128-token tiles as T grows (up to 32 x SMs, 64 x
+# SMs, beyond): odd expert counts (rows past E of its 128-row tile), bias, no
+# renorm, k up to 32, ragged last tiles.
 @pytest.mark.parametrize("T,H,E,k,renorm,bias", [
-    (4097, 64, 33, 7, True, True), (4500, 128, 128, 8, False, False),
-    (5000, 192, 97, 32, True, False), (8192, 64, 64, 1, False, True),
+    (65, 128, 128, 8, True, False), (4097, 64, 33, 7, True, True),
+    (4500, 128, 128, 8, False, False), (5000, 192, 97, 32, True, False),
+    (12001, 64, 64, 1, False, True), (20000, 64, 120, 6, True, True),
 ])
 def test_route_tensor_core_shapes(T, H, E, k, renorm, bias):
     d = random_small_inputs(T + E + k, T, H, E, 64, bias=bias)
     _check_route(d["hidden"], d["router_w"], d["router_bias"], k, renorm)
 
 
-def test_route_tensor_core_forced_ties():
-    # As below, at a batch size that takes the tensor-core router: exact ties
-    # between experts of both halves of each thread pair's split.
-    T, H, E, k = 4200, 64, 128, 8
+@pytest.mark.parametrize("T", [4200, 8000, 20000])
+def test_route_tensor_core_forced_ties(T):
+    # As below, at batch sizes that take the tensor-core router with each
+    # token-tile size: exact ties between experts held by different threads
+    # of the group that finishes a token.
+    H, E, k = 64, 128, 8
     c = (np.arange(E) % 5 + 1).astype(np.float64)  # values 1..5, each ~26 times
     bias = np.log(c).astype(np.float32)
     hidden = random_small_inputs(7, T, H, E, 64)["hidden"]
