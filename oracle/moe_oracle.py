@@ -19,6 +19,9 @@ float64 variant of the expert loop and a dense brute force for pinning it):
   align    token batching by expert: a stable, block-padded grouping of the
            flat (token, slot) ids by expert ("mini-sglang guide, chapter 7",
            paragraph on ``moe/fused.py``).
+  norm     the residual add + RMSNorm before the MoE ("mini-sglang guide",
+           the decoder layer, RMSNormFused and the torch_ops ``rmsnorm`` /
+           ``fused_add_rmsnorm``), in the pages' rounding order.
   experts  per expert: gate_up projection, SiLU(gate) * up, down projection
            ("模型与权重加载", GatedMLP: gate_up_proj -> silu_and_mul ->
            down_proj, gate rows before up rows; streaming loader, step 4:
@@ -33,7 +36,9 @@ sentinel = T*k; rows [0, I) of w_gate_up[e] are gate, [I, 2I) are up.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
 closed forms, invariants, brute force over all k-subsets, a dense masked
-formulation and the textbook dense SwiGLU MLP. No function is unpinned.
+formulation, the textbook dense SwiGLU MLP, torch's bf16 cast and bf16 add,
+torch's float64 rms_norm, and a hand-worked add + RMSNorm example
+(``tests/golden/add_rmsnorm_worked.json``). No function is unpinned.
 """
 from __future__ import annotations
 
@@ -47,6 +52,71 @@ def widen_bf16(bits: np.ndarray) -> np.ndarray:
     of an IEEE binary32)."""
     b = np.asarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """float32 -> bit pattern (uint16) of the nearest bf16, ties to even
+    (what a cast to bf16 does); NaN stays NaN. Written out on the integer
+    bits: add half an ulp of the dropped 16 bits, plus one when the kept part
+    is odd (so an exact half rounds to even), then drop them."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    out = rounded.astype(np.uint16)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    out[nan] = ((b[nan] >> np.uint64(16)) | np.uint64(0x40)).astype(np.uint16)  # quiet NaN
+    return out
+
+
+# ------------------------------------------------------ add + RMSNorm ---
+#
+# The step before the MoE in a decoder layer ("mini-sglang guide", decoder
+# layer and RMSNormFused; torch_ops ``rmsnorm`` / ``fused_add_rmsnorm``):
+# residual <- x + residual (in the bf16 dtype of the tensors); then
+# y = r * rsqrt(mean(r^2) + eps) in float32, rounded to bf16, times the
+# weight, rounded to bf16. The pages leave the order of the float32 sum of
+# squares open; the reading taken (design notes) fixes it as: lane l of 32
+# sums, in order, its 8-element chunks c = l, l + 32, l + 64, ... (elements
+# 8c .. 8c+7 in order, each square rounded before the add), then the 32 lane
+# sums are combined by an xor butterfly (offsets 16, 8, 4, 2, 1). rsqrt(v)
+# is read as 1 / sqrt(v), each step rounded to float32.
+
+def sum_of_squares(xf: np.ndarray) -> np.ndarray:
+    """Float32 sum over the last axis of xf**2, in the order stated above."""
+    xf = np.asarray(xf, dtype=np.float32)
+    H = xf.shape[-1]
+    Hp = -(-H // 256) * 256
+    sq = np.zeros(xf.shape[:-1] + (Hp,), dtype=np.float32)
+    sq[..., :H] = xf * xf  # float32 products; zero padding adds exactly 0
+    sq = sq.reshape(xf.shape[:-1] + (Hp // 256, 32, 8))  # [.., round i, lane, element]
+    lanes = np.zeros(xf.shape[:-1] + (32,), dtype=np.float32)
+    for i in range(Hp // 256):
+        for e in range(8):
+            lanes = lanes + sq[..., i, :, e]
+    for o in (16, 8, 4, 2, 1):
+        lanes = lanes + lanes[..., np.arange(32) ^ o]
+    return lanes[..., 0]
+
+
+def rmsnorm(x_bits: np.ndarray, weight_bits: np.ndarray, eps: float) -> np.ndarray:
+    """bf16 rows x [.., H], bf16 weight [H] -> bf16 bit patterns of
+    weight * bf16(x * rsqrt(mean(x^2) + eps))."""
+    xf = widen_bf16(x_bits)
+    H = xf.shape[-1]
+    mean = sum_of_squares(xf) / np.float32(H)
+    inv = np.float32(1.0) / np.sqrt(mean + np.float32(eps), dtype=np.float32)
+    y = round_bf16(xf * inv[..., None])
+    return round_bf16(widen_bf16(weight_bits)[None, :] * widen_bf16(y))
+
+
+def fused_add_rmsnorm(x_bits, residual_bits, weight_bits, eps: float):
+    """Returns (normalised rows, new residual), both bf16 bit patterns:
+    residual' = bf16(x + residual); normalised = rmsnorm(residual'). With
+    residual None (the first layer) x itself is the residual."""
+    if residual_bits is None:
+        r = np.asarray(x_bits, dtype=np.uint16).copy()
+    else:
+        r = round_bf16(widen_bf16(x_bits) + widen_bf16(residual_bits))
+    return rmsnorm(r, weight_bits, eps), r
 
 
 # --------------------------------------------------------------- routing ---
@@ -221,3 +291,12 @@ def moe_layer(inputs: dict, top_k: int, renorm: bool, block_m: int = 16,
     return {"topk_ids": ids, "topk_w": w, "logits": logits,
             "sorted_token_ids": sorted_ids, "expert_offsets": offsets,
             "expert_counts": counts, "out": out}
+
+
+def moe_layer_after_norm(inputs: dict, x_bits, residual_bits, norm_w_bits, eps: float,
+                         top_k: int, renorm: bool, block_m: int = 16) -> dict:
+    """The MoE layer fed by the add + RMSNorm step before it: returns the
+    normalised rows, the new residual and every output of moe_layer on them."""
+    xn, r = fused_add_rmsnorm(x_bits, residual_bits, norm_w_bits, eps)
+    res = moe_layer({**inputs, "hidden": xn}, top_k, renorm, block_m)
+    return {**res, "normed": xn, "residual": r}

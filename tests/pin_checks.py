@@ -42,6 +42,112 @@ def check_widen_bf16():
 
 # -------------------------------------------------------------- routing ---
 
+# ------------------------------------------------------ bf16 rounding ---
+
+def check_round_bf16():
+    # Worked values: exact, ties to even (1 + 2^-8 sits halfway between 1 and
+    # 1 + 2^-7), a tie that rounds up to the even neighbour, sign, inf, NaN.
+    x = np.array([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.5, np.inf, -0.0],
+                 dtype=np.float32)
+    want = [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x7F80, 0x8000]
+    assert O.round_bf16(x).tolist() == want
+    assert np.isnan(O.widen_bf16(O.round_bf16(np.array([np.nan], dtype=np.float32))))[0]
+    # Library routine: torch's float32 -> bfloat16 cast (round to nearest even),
+    # on random values and on random bit patterns (NaNs excluded).
+    import torch
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([rng.standard_normal(20000).astype(np.float32) * 3,
+                           rng.integers(0, 2 ** 32, 20000, dtype=np.uint64)
+                           .astype(np.uint32).view(np.float32)])
+    vals = vals[~np.isnan(vals)]
+    lib = torch.from_numpy(vals.copy()).to(torch.bfloat16).view(torch.int16).numpy()
+    assert np.array_equal(O.round_bf16(vals), lib.view(np.uint16))
+
+
+# ------------------------------------------------------ add + RMSNorm ---
+
+def check_sum_of_squares():
+    rng = np.random.default_rng(12)
+    # Small integers: every partial sum is an exact float32 integer, so any
+    # summation order gives the exact sum.
+    for H in (64, 192, 2048, 4096):
+        x = rng.integers(-3, 4, size=(5, H)).astype(np.float32)
+        assert np.array_equal(O.sum_of_squares(x), (x.astype(np.int64) ** 2).sum(1)
+                              .astype(np.float32))
+    # Random rows: within the float32 error bound of a sum of n terms
+    # (n - 1 additions, each off by at most half an ulp of the partial sum).
+    x = rng.standard_normal((7, 4096)).astype(np.float32)
+    got = O.sum_of_squares(x).astype(np.float64)
+    exact = np.array([math.fsum((r.astype(np.float64) ** 2).tolist()) for r in x])
+    assert (np.abs(got - exact) <= 4096 * 2.0 ** -24 * exact).all()
+
+
+def _textbook_rmsnorm(r_bits, w_bits, eps):
+    """float64 weight * x / sqrt(mean(x^2) + eps) via torch's rms_norm."""
+    import torch
+    xf = torch.from_numpy(O.widen_bf16(r_bits).astype(np.float64))
+    wf = torch.from_numpy(O.widen_bf16(w_bits).astype(np.float64))
+    return torch.nn.functional.rms_norm(xf, (xf.shape[-1],), wf, eps).numpy()
+
+
+def check_rmsnorm_golden():
+    g = json.load(open(os.path.join(GOLDEN, "add_rmsnorm_worked.json")))
+    def row(d):
+        return np.concatenate([np.full(n, int(b, 16), dtype=np.uint16) for b, n in d.items()])
+    x, res = row(g["x_bits"])[None, :], row(g["residual_bits"])[None, :]
+    w = np.full(g["H"], int(g["weight_bits"], 16), dtype=np.uint16)
+    normed, r = O.fused_add_rmsnorm(x, res, w, g["eps"])
+    assert np.array_equal(r[0], row(g["residual_out_bits"]))
+    assert np.array_equal(normed[0], row(g["normed_bits"]))
+    assert np.array_equal(O.rmsnorm(r, w, g["eps"]), normed)
+
+
+def check_rmsnorm_closed_forms():
+    rng = np.random.default_rng(13)
+    H = 256
+    w = _bf16(rng.uniform(0.5, 1.5, H))
+    # Constant rows c * 1 with c a power of two, eps = 0: the row normalises
+    # to sign(c) exactly, so the output is the weight with c's sign.
+    for c in (0.25, -4.0, 1.0):
+        out = O.rmsnorm(_bf16(np.full((1, H), c)), w, 0.0)
+        assert np.array_equal(O.widen_bf16(out)[0], np.sign(c) * O.widen_bf16(w))
+    # Scale invariance: with eps = 0 scaling a row by a power of two scales
+    # every intermediate exactly, so the output is bit-identical.
+    x = _bf16(rng.standard_normal((4, H)))
+    for a in (2.0 ** -3, 2.0 ** 5):
+        xs = _bf16(O.widen_bf16(x) * np.float32(a))
+        assert np.array_equal(O.rmsnorm(xs, w, 0.0), O.rmsnorm(x, w, 0.0))
+    # A zero row with eps > 0 gives zeros (no 0/0).
+    assert not O.widen_bf16(O.rmsnorm(np.zeros((1, H), np.uint16), w, 1e-6)).any()
+    # The textbook float64 RMSNorm (torch's rms_norm), within the two bf16
+    # roundings; eps = 1 on small rows makes eps carry weight.
+    for eps, scale in ((1e-6, 1.0), (1.0, 0.3)):
+        x = _bf16(rng.standard_normal((6, H)) * scale)
+        ref = _textbook_rmsnorm(x, w, eps)
+        got = O.widen_bf16(O.rmsnorm(x, w, eps)).astype(np.float64)
+        assert (np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30).all()
+
+
+def check_fused_add_rmsnorm():
+    rng = np.random.default_rng(14)
+    T, H = 5, 192
+    x = _bf16(rng.standard_normal((T, H)))
+    res = _bf16(rng.standard_normal((T, H)) * 4)
+    w = _bf16(rng.uniform(0.5, 1.5, H))
+    normed, r = O.fused_add_rmsnorm(x, res, w, 1e-6)
+    # The residual add is torch's bf16 add (one rounding of the exact sum).
+    import torch
+    tb = lambda b: torch.from_numpy(b.view(np.int16).copy()).view(torch.bfloat16)
+    lib = (tb(x) + tb(res)).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(r, lib)
+    assert np.array_equal(normed, O.rmsnorm(r, w, 1e-6))
+    n2, r2 = O.fused_add_rmsnorm(res, x, w, 1e-6)  # the add is symmetric
+    assert np.array_equal(n2, normed) and np.array_equal(r2, r)
+    # First layer: no residual yet, x is the residual.
+    n0, r0 = O.fused_add_rmsnorm(x, None, w, 1e-6)
+    assert np.array_equal(r0, x) and np.array_equal(n0, O.rmsnorm(x, w, 1e-6))
+
+
 def check_router_logits_one_hot():
     # x[t] = e_{h_t}: logit[t, e] must be Wr[e, h_t] (+ bias[e]) exactly.
     rng = np.random.default_rng(1)

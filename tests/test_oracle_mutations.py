@@ -10,7 +10,8 @@ from oracle import moe_oracle as O
 
 _orig = {n: getattr(O, n) for n in ("silu_and_mul", "select_topk", "routing_weights",
                                     "softmax_over_experts", "router_logits", "align",
-                                    "experts_loop", "widen_bf16")}
+                                    "experts_loop", "widen_bf16", "round_bf16",
+                                    "sum_of_squares", "rmsnorm", "fused_add_rmsnorm")}
 
 
 def _swap_gate_up(g, u):
@@ -115,7 +116,55 @@ def _widen_truncate(bits):
     return v
 
 
+def _round_truncate(x):
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _round_ties_up(x):
+    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
+
+
+def _sumsq_drop_last(xf):
+    return _orig["sum_of_squares"](np.asarray(xf)[..., :-1])
+
+
+def _rms_no_eps(x, w, eps):
+    return _orig["rmsnorm"](x, w, 0.0)
+
+
+def _rms_sum_not_mean(x, w, eps):
+    xf = O.widen_bf16(x)
+    inv = np.float32(1.0) / np.sqrt(O.sum_of_squares(xf) + np.float32(eps), dtype=np.float32)
+    y = O.round_bf16(xf * inv[..., None])
+    return O.round_bf16(O.widen_bf16(w)[None, :] * O.widen_bf16(y))
+
+
+def _rms_single_round(x, w, eps):
+    xf = O.widen_bf16(x)
+    mean = O.sum_of_squares(xf) / np.float32(xf.shape[-1])
+    inv = np.float32(1.0) / np.sqrt(mean + np.float32(eps), dtype=np.float32)
+    return O.round_bf16(O.widen_bf16(w)[None, :] * (xf * inv[..., None]))
+
+
+def _add_ignores_residual(x, r, w, eps):
+    return _orig["fused_add_rmsnorm"](x, None, w, eps)
+
+
+def _add_keeps_old_residual(x, r, w, eps):
+    normed, _ = _orig["fused_add_rmsnorm"](x, r, w, eps)
+    return normed, (x if r is None else r)
+
+
 MUTANTS = {
+    "round_truncate": ("round_bf16", _round_truncate),
+    "round_ties_up": ("round_bf16", _round_ties_up),
+    "sumsq_drop_last": ("sum_of_squares", _sumsq_drop_last),
+    "rms_no_eps": ("rmsnorm", _rms_no_eps),
+    "rms_sum_not_mean": ("rmsnorm", _rms_sum_not_mean),
+    "rms_single_round": ("rmsnorm", _rms_single_round),
+    "add_ignores_residual": ("fused_add_rmsnorm", _add_ignores_residual),
+    "add_keeps_old_residual": ("fused_add_rmsnorm", _add_keeps_old_residual),
     "swap_gate_up": ("silu_and_mul", _swap_gate_up),
     "silu_sign": ("silu_and_mul", _silu_sign),
     "tie_high_id": ("select_topk", _tie_high_id),
