@@ -217,6 +217,79 @@ def cpu_baseline(shape, budget_s: float):
                       f"({dt:.1f} s, numpy fp32 with OpenBLAS threads)"}
 
 
+def run_dense(args, shape, ws, rank, dev, mm):
+    """Times mm_gated_mlp on the workload's T tokens: a dense SwiGLU MLP with
+    hidden H and intermediate k*I, the flops per token of the MoE layer's
+    experts. Same timing rules as the layer (warm-up, events, NVML clocks,
+    max over ranks); the roofline is taken over the whole call."""
+    T, H, I = shape.T, shape.H, shape.top_k * shape.I
+    w = synthetic.make_dense_weights(0, H, I)
+    x_np = synthetic.make_hidden(synthetic.MoEShape(**{**shape.__dict__, "seed": rank}))
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, wgu, wdn = to_dev(x_np), to_dev(w["w_gate_up"]), to_dev(w["w_down"])
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd = lambda: mm.mm_gated_mlp(x, wgu, wdn, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    if args.steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            fwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        args.steps = int(min(5000, max(20, 600.0 / max(e0.elapsed_time(e1) / 5, 1e-3))))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            fwd()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    ms = t_start.elapsed_time(t_end) / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    st = mm.mm_poll_device_status()
+    if st != mm.MM_OK:
+        raise RuntimeError(f"device status after the timed region: {mm.status_string(st)}")
+    flops = 2 * T * H * 2 * I + 2 * T * I * H
+    nbytes = 3 * H * I * 2 + 2 * T * H * 2
+    pk, pk_kind = peaks()
+    tensor = flops / nbytes > pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if tensor:
+        ach = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"], "peak_kind": f"{pk_kind} bf16_tflops (burst)"}
+    else:
+        ach = nbytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)"}
+    roof["kernel"] = "mm_gated_mlp, whole call (grouping, gate_up, down, finalize)"
+    roof["traffic"] = None
+    line = {"metric": "dense SwiGLU MLP tokens/s", "value": T * ws / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
+            "config": {"workload": f"dense_gated_mlp_T{T}_H{H}_I{I}", "T": T, "H": H, "I": I,
+                       "parallelism": f"replicas x{ws}",
+                       "l2": f"weights {3 * H * I * 2 / 1e6:.0f} MB per step"},
+            "roofline": roof, "gpu_launches": 4 * args.steps, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -229,6 +302,12 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--add-norm", action="store_true",
+                    help="time mm_moe_forward_add_norm: the residual add + RMSNorm step "
+                         "before the layer, then the layer, in one call")
+    ap.add_argument("--dense", action="store_true",
+                    help="time mm_gated_mlp: a dense SwiGLU MLP of H x k*I on the workload's "
+                         "tokens (the same flops per token as the MoE layer's experts)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -254,6 +333,11 @@ def main():
     mm.lib()  # fails loudly if the CUDA library is missing
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.dense:
+        run_dense(args, shape, ws, rank, dev, mm)
+        return
+    if args.add_norm and synthetic.make_router_bias(shape) is not None:
+        raise SystemExit("--add-norm takes no router bias (the Zipf sweep has one)")
     # Each replica gets its own batch (hidden seed = rank); the layer weights are shared.
     w = synthetic.make_weights(shape)
     hid_np = synthetic.make_hidden(synthetic.MoEShape(**{**shape.__dict__, "seed": rank}))
@@ -272,6 +356,15 @@ def main():
 
     def fwd():
         mm.mm_moe_forward(hidden, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
+
+    eps = 1e-6
+    if args.add_norm:  # x, the residual stream and the norm weight of the step before
+        nrm = synthetic.make_norm_inputs(rank, shape.T, shape.H)
+        x_d, res_d, nw_d = to_dev(nrm["x"]), to_dev(nrm["residual"]), to_dev(nrm["norm_w"])
+
+        def fwd():  # noqa: F811 - the timed call in this mode
+            mm.mm_moe_forward_add_norm(x_d, nw_d, eps, router_w, w_gu, w_dn, k, renorm,
+                                       residual=res_d, out=out)
 
     def barrier():
         if ws > 1:
@@ -359,6 +452,10 @@ def main():
     h_host.copy_(hidden.cpu())
     o_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
     h_dev = torch.empty_like(hidden)
+    if args.add_norm:  # the step's inputs are x and the residual; outputs out and residual
+        r_host = torch.empty_like(h_host, pin_memory=True)
+        r_host.copy_(res_d.cpu())
+        r_back = torch.empty_like(h_host, pin_memory=True)
     barrier()
     torch.cuda.synchronize()
     e2e_total = 0.0
@@ -369,7 +466,13 @@ def main():
             stream.synchronize()
             t0 = time.perf_counter()
         h_dev.copy_(h_host, non_blocking=True)
-        mm.mm_moe_forward(h_dev, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
+        if args.add_norm:
+            res_d.copy_(r_host, non_blocking=True)
+            mm.mm_moe_forward_add_norm(h_dev, nw_d, eps, router_w, w_gu, w_dn, k, renorm,
+                                       residual=res_d, out=out)
+            r_back.copy_(res_d, non_blocking=True)
+        else:
+            mm.mm_moe_forward(h_dev, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
         o_host.copy_(out, non_blocking=True)
         stream.synchronize()
         if flush:
@@ -406,13 +509,15 @@ def main():
     single_align = shape.T <= 1024 and shape.T * k <= 8192
     rows_gathered = shape.T * k > 64 * shape.E  # token rows copied into segment order
     launches_per_step = (4 + (0 if fused_align else 1 if single_align else 2)
-                         + (1 if rows_gathered else 0))
+                         + (1 if rows_gathered else 0) + (1 if args.add_norm else 0))
+    n_io = 2 if args.add_norm else 1  # x and residual in, out and residual back
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded normals, bf16; random-init weights of the named shape)",
-            "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "E": shape.E,
+            "config": {"workload": shape.name + ("+add_rmsnorm" if args.add_norm else ""),
+                       "T": shape.T, "H": shape.H, "E": shape.E,
                        "top_k": k, "I": shape.I, "renorm": renorm,
                        "distinct_experts": work["D"], "parallelism": f"replicas x{ws}",
                        "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write "
@@ -425,8 +530,8 @@ def main():
             "stage_ms": {n: round(v, 5) for n, v in stage_ms.items()},
             "stage_sum_ms": layer_ms,
             "e2e": {"value": T_all / e2e_s, "unit": UNIT,
-                    "h2d_bytes_per_step": int(h_host.numel() * 2),
-                    "d2h_bytes_per_step": int(o_host.numel() * 2)},
+                    "h2d_bytes_per_step": int(h_host.numel() * 2 * n_io),
+                    "d2h_bytes_per_step": int(o_host.numel() * 2 * n_io)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
     if rank == 0 and not args.no_cpu_baseline:

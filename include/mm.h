@@ -212,6 +212,37 @@ int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16
 int64_t mm_gated_mlp_workspace_size(int T, int H, int I);
 
 /*
+ * The residual add + RMSNorm that precedes the MoE block in a decoder layer
+ * ("mini-sglang guide": the decoder layer's post_attention_layernorm,
+ * RMSNormFused, and the torch_ops rmsnorm / fused_add_rmsnorm listings):
+ *   residual' = bf16(x + residual)                  (written back to residual)
+ *   normed    = bf16(norm_w * bf16(residual' * rsqrt(mean(residual'^2) + eps)))
+ * With residual == NULL (the first layer) x is the residual and is only read.
+ * The float32 sum of squares runs in a fixed order (32 lanes each summing
+ * the 8-element chunks c = lane, lane + 32, ... in order, then an xor
+ * butterfly) and rsqrt is 1/sqrt with both steps rounded, so normed is
+ * bit-reproducible.
+ *
+ * x, residual, normed [T,H] bf16 row-major; norm_w [H] bf16; eps >= 0.
+ * Caller-owned device pointers, 16-byte aligned; x, residual and normed must
+ * not overlap. H % 64 != 0 -> MM_ERR_UNSUPPORTED. T == 0 is a no-op.
+ */
+int mm_add_rmsnorm(const uint16_t* x, uint16_t* residual, const uint16_t* norm_w, float eps,
+                   int T, int H, uint16_t* normed, void* stream);
+
+/*
+ * The MoE layer behind that step, in one call: residual' and normed as in
+ * mm_add_rmsnorm (normed kept in the library's workspace), then
+ * out = mm_moe_forward(normed, ...). Same arguments as mm_moe_forward plus
+ * x / residual / norm_w / eps (no router bias). The kernels run back to back
+ * on `stream`; the normed rows never leave the library.
+ */
+int mm_moe_forward_add_norm(const uint16_t* x, uint16_t* residual, const uint16_t* norm_w,
+                            float eps, const uint16_t* router_w, const uint16_t* w_gate_up,
+                            const uint16_t* w_down, int T, int H, int E, int I, int top_k,
+                            int renorm, uint16_t* out, void* stream);
+
+/*
  * Stage timing of mm_moe_forward_ex, for profiling. Same arguments, plus
  * `events`: a host array of MM_PROFILE_EVENTS cudaEvent_t handles (created
  * by the caller with timing enabled). events[i] is recorded on `stream`

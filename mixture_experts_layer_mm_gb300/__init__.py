@@ -8,7 +8,8 @@ synthetic inputs shared with the tests (``synthetic``).
 from ._lib import (  # noqa: F401
     FORWARD_BLOCK_M, LIB_PATH, MM_ERR_CUDA, MM_ERR_DEVICE, MM_ERR_INVALID_ARG,
     MM_ERR_NO_MEMORY, MM_ERR_TIMEOUT, MM_ERR_UNSUPPORTED, MM_GEMM_DOWN, MM_GEMM_GATE_UP,
-    MM_OK, MMError, SIGNATURES, lib, mm_align, mm_align_capacity, mm_align_noalloc, mm_grouped_gemm,
-    mm_gated_mlp, mm_gated_mlp_workspace_size, mm_moe_forward, mm_moe_forward_profiled, mm_moe_workspace_size, PROFILE_STAGES, mm_poll_device_status, mm_route, mm_shutdown,
-    status_string,
+    MM_OK, PROFILE_STAGES, MMError, SIGNATURES, lib, mm_add_rmsnorm, mm_align,
+    mm_align_capacity, mm_align_noalloc, mm_gated_mlp, mm_gated_mlp_workspace_size,
+    mm_grouped_gemm, mm_moe_forward, mm_moe_forward_add_norm, mm_moe_forward_profiled,
+    mm_moe_workspace_size, mm_poll_device_status, mm_route, mm_shutdown, status_string,
 )

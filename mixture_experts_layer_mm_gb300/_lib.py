@@ -42,6 +42,9 @@ SIGNATURES = {
                                      _P]),
     "mm_gated_mlp": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "mm_gated_mlp_workspace_size": (_I64, [_I, _I, _I]),
+    "mm_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _I, _I, _P, _P]),
+    "mm_moe_forward_add_norm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, _I, _I,
+                                     _I, _P, _P]),
     "mm_poll_device_status": (_I, [_P]),
     "mm_shutdown": (None, []),
 }
@@ -226,6 +229,41 @@ def mm_gated_mlp(hidden, w_gate_up, w_down, out=None, stream=None):
                               _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
                               _ptr(w_down, torch.bfloat16, "w_down"), T, H, I,
                               _ptr(out, torch.bfloat16, "out"), _stream(stream)), "mm_gated_mlp")
+    return out
+
+
+def mm_add_rmsnorm(x, norm_w, eps: float, residual=None, normed=None, stream=None):
+    """residual <- bf16(x + residual) in place (residual None: x is the
+    residual); returns normed = rmsnorm(residual, norm_w, eps) [T, H] bf16."""
+    T, H = x.shape
+    if normed is None:
+        normed = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mm_add_rmsnorm(_ptr(x, torch.bfloat16, "x"),
+                                _ptr(residual, torch.bfloat16, "residual"),
+                                _ptr(norm_w, torch.bfloat16, "norm_w"), float(eps), T, H,
+                                _ptr(normed, torch.bfloat16, "normed"), _stream(stream)),
+           "mm_add_rmsnorm")
+    return normed
+
+
+def mm_moe_forward_add_norm(x, norm_w, eps: float, router_w, w_gate_up, w_down, top_k: int,
+                            renorm: bool, residual=None, out=None, stream=None):
+    """The MoE layer on rmsnorm(x + residual) (residual updated in place, or
+    x itself when residual is None); returns out [T, H] bf16."""
+    T, H = x.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _check(lib().mm_moe_forward_add_norm(_ptr(x, torch.bfloat16, "x"),
+                                         _ptr(residual, torch.bfloat16, "residual"),
+                                         _ptr(norm_w, torch.bfloat16, "norm_w"), float(eps),
+                                         _ptr(router_w, torch.bfloat16, "router_w"),
+                                         _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+                                         _ptr(w_down, torch.bfloat16, "w_down"), T, H, E, I,
+                                         top_k, int(bool(renorm)),
+                                         _ptr(out, torch.bfloat16, "out"), _stream(stream)),
+           "mm_moe_forward_add_norm")
     return out
 
 

@@ -81,7 +81,7 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
+  size_t normed, ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
   long long capacity;
   bool rows_in_order;  // token rows are copied into segment order before gate_up
 };
@@ -89,7 +89,9 @@ struct ForwardLayout {
 // gather_rows: whether a gate_up with many rows per expert reads a copy of
 // the token rows in segment order (the MoE layer); a dense MLP's rows are in
 // order already.
-ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows = true) {
+// normed: room for the rows the add + RMSNorm step hands to the layer.
+ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows = true,
+                             bool normed = false) {
   ForwardLayout L;
   L.capacity = (long long)T * k + (long long)E * (kForwardBlockM - 1);
   size_t off = 0;
@@ -98,6 +100,7 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows
     off += round256(bytes);
     return o;
   };
+  L.normed = take(normed ? (size_t)T * H * 2 : 0);
   L.ids = take((size_t)T * k * 4);
   L.w = take((size_t)T * k * 4);
   L.sorted = take((size_t)L.capacity * 4);
@@ -161,7 +164,7 @@ int mm_route(const uint16_t* hidden, const uint16_t* router_w, const float* rout
   DevState* s = nullptr;
   if ((rc = device_state(&s)) != MM_OK) return rc;
   return cuda_status(launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, topk_ids,
-                                  topk_w, nullptr, 0, nullptr, s->sms, s->status,
+                                  topk_w, nullptr, 0, nullptr, s->sms, s->status, false,
                                   static_cast<cudaStream_t>(stream)));
 }
 
@@ -223,13 +226,24 @@ int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
 
 namespace {
 
+// The add + RMSNorm step before the layer (see mm_moe_forward_add_norm).
+struct NormIn {
+  const uint16_t* x;
+  uint16_t* residual;  // NULL: x is the residual
+  const uint16_t* weight;
+  float eps;
+};
+
 // The launch sequence of the layer. If `ev` is non-null, events ev[0..5] are
 // recorded on the stream around the stages: route (which also groups the
 // tokens when T <= 64) | align (empty then) | gate_up | down | finalize.
+// With `norm`, hidden is ignored: a first kernel writes rmsnorm(x + residual)
+// into the workspace and the layer reads it.
 int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
-                 cudaStream_t st, cudaEvent_t const* ev) {
+                 cudaStream_t st, cudaEvent_t const* ev, const NormIn* norm = nullptr) {
+  if (norm != nullptr) hidden = norm->x;  // for the checks below
   int rc = check_route_shape(T, H, E, top_k);
   if (rc != MM_OK) return rc;
   if (I <= 0) return MM_ERR_INVALID_ARG;
@@ -239,7 +253,10 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(w_gate_up) ||
       !aligned16(w_down) || !aligned16(out))
     return MM_ERR_INVALID_ARG;
-  const ForwardLayout L = forward_layout(T, H, E, I, top_k);
+  if (norm != nullptr && (!norm->weight || !aligned16(norm->weight) ||
+                          (norm->residual && !aligned16(norm->residual)) || !(norm->eps >= 0.f)))
+    return MM_ERR_INVALID_ARG;
+  const ForwardLayout L = forward_layout(T, H, E, I, top_k, true, norm != nullptr);
   if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
   if (workspace != nullptr) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MM_ERR_INVALID_ARG;
@@ -265,10 +282,17 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
 
   if (!mark(0)) return MM_ERR_CUDA;
+  if (norm != nullptr) {
+    uint16_t* normed = at<uint16_t>(ws, L.normed);
+    if (launch_add_rmsnorm(norm->x, norm->residual, norm->weight, norm->eps, T, H, normed, s->sms,
+                           false, st) != cudaSuccess)
+      return MM_ERR_CUDA;
+    hidden = normed;
+  }
   const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
   const bool fused = route_fuses_align(T, top_k);
   if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, &fa,
-                   s->sms, s->status, st) != cudaSuccess ||
+                   s->sms, s->status, norm != nullptr, st) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
   if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
@@ -366,6 +390,32 @@ int mm_gated_mlp(const uint16_t* hidden, const uint16_t* w_gate_up, const uint16
                           L.capacity, L.capacity, s->sms, s->status, true, st) != cudaSuccess)
     return MM_ERR_CUDA;
   return cuda_status(launch_finalize(acc, out, nacc, s->sms, true, st));
+}
+
+int mm_add_rmsnorm(const uint16_t* x, uint16_t* residual, const uint16_t* norm_w, float eps,
+                   int T, int H, uint16_t* normed, void* stream) {
+  if (T < 0 || H <= 0 || !(eps >= 0.f)) return MM_ERR_INVALID_ARG;
+  if (H % 64 != 0) return MM_ERR_UNSUPPORTED;
+  if (T == 0) return MM_OK;
+  if (!x || !norm_w || !normed) return MM_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(norm_w) || !aligned16(normed) ||
+      (residual && !aligned16(residual)))
+    return MM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  return cuda_status(launch_add_rmsnorm(x, residual, norm_w, eps, T, H, normed, s->sms, false,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int mm_moe_forward_add_norm(const uint16_t* x, uint16_t* residual, const uint16_t* norm_w,
+                            float eps, const uint16_t* router_w, const uint16_t* w_gate_up,
+                            const uint16_t* w_down, int T, int H, int E, int I, int top_k,
+                            int renorm, uint16_t* out, void* stream) {
+  const NormIn norm = {x, residual, norm_w, eps};
+  return forward_impl(nullptr, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                      out, nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, &norm);
 }
 
 int mm_poll_device_status(void* stream) {

@@ -75,7 +75,7 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
                          const AlignOut* fuse_align, int num_sms, unsigned* err,
-                         cudaStream_t st);
+                         bool after_prev, cudaStream_t st);
 
 // Whether launch_route runs the tensor-core router (route_tc.cu) for this
 // batch, and that router's launcher (same arguments, no grouping).
@@ -83,7 +83,7 @@ bool route_uses_tensor_cores(int T, int E);
 cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                             int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                             float* topk_w, float* zero_buf, long long zero_count, int num_sms,
-                            unsigned* err, cudaStream_t st);
+                            unsigned* err, bool after_prev, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);
@@ -128,5 +128,11 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
                             bool after_prev, cudaStream_t st);
+
+// residual' = bf16(x + residual) in place (residual NULL: x is the residual),
+// normed = rmsnorm(residual', weight, eps) [T, H] bf16. H % 8 == 0.
+cudaError_t launch_add_rmsnorm(const uint16_t* x, uint16_t* residual, const uint16_t* weight,
+                               float eps, int T, int H, uint16_t* normed, int num_sms,
+                               bool after_prev, cudaStream_t st);
 
 }  // namespace mm

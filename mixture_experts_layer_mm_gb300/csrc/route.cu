@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
+  pdl_wait();  // hidden may come from the kernel before this one (the RMSNorm step)
   pdl_trigger();  // the next kernel of the layer may be scheduled (it waits for this one)
   const int t0 = (blockIdx.x / ks) * kRtTok;
   const int hs = H / ks, hbase = (int)rank * hs;
@@ -238,7 +239,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
 template <int EP>
 cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                       int H, int E, int top_k, int renorm, int32_t* ids, float* w, float* zero_buf,
-                      long long zero_count, const AlignOut& fa, int num_sms, cudaStream_t st) {
+                      long long zero_count, const AlignOut& fa, int num_sms, bool after_prev,
+                      cudaStream_t st) {
   const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
   const size_t recv_bytes = (size_t)kRtTok * EP * sizeof(float);
   const size_t smem = gemm_bytes > recv_bytes ? gemm_bytes : recv_bytes;
@@ -267,13 +269,15 @@ cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const fl
   cfg.blockDim = dim3(kRtThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = after_prev ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, route_kernel<EP>, hidden, router_w, bias, T, H, E, top_k, renorm,
                             ks, ids, w, zero_buf, zero_count, fa);
 }
@@ -286,24 +290,24 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
                          const AlignOut* fuse_align, int num_sms, unsigned* err,
-                         cudaStream_t st) {
+                         bool after_prev, cudaStream_t st) {
   // More than one 64-token tile and at most 128 experts: the tcgen05 router.
   if (route_uses_tensor_cores(T, E))
     return launch_route_tc(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                           zero_buf, zero_count, num_sms, err, st);
+                           zero_buf, zero_count, num_sms, err, after_prev, st);
   AlignOut fa = {};
   if (fuse_align != nullptr && route_fuses_align(T, top_k)) fa = *fuse_align;
   if (E <= 32)
     return launch_ep<32>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, fa, num_sms, st);
+                         zero_buf, zero_count, fa, num_sms, after_prev, st);
   if (E <= 64)
     return launch_ep<64>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, fa, num_sms, st);
+                         zero_buf, zero_count, fa, num_sms, after_prev, st);
   if (E <= 128)
     return launch_ep<128>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, fa, num_sms, st);
+                          zero_buf, zero_count, fa, num_sms, after_prev, st);
   return launch_ep<256>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w, zero_buf,
-                        zero_count, fa, num_sms, st);
+                        zero_count, fa, num_sms, after_prev, st);
 }
 
 }  // namespace mm

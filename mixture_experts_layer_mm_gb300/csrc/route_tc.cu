@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tiles = (T + TOK - 1) / TOK;
+  pdl_wait();  // hidden may come from the kernel before this one (the RMSNorm step)
   pdl_trigger();  // the next kernel of the layer may be scheduled (it waits for this one)
   if ((int)blockIdx.x >= tiles) {  // no tile: this CTA only clears its slice
     zero_slice(zero_buf, zero_count, tid, kRcThreads);
@@ -387,7 +388,7 @@ template <int TOK>
 cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                        int H, int E, int top_k, int renorm, int32_t* ids, float* w,
                        float* zero_buf, long long zero_count, int num_sms, unsigned* err,
-                       cudaStream_t st) {
+                       bool after_prev, cudaStream_t st) {
   using Cfg = RcCfg<TOK>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -405,8 +406,8 @@ cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const f
   const int grid = zero_buf != nullptr ? (tiles > num_sms ? tiles : num_sms)
                                        : (tiles < num_sms ? tiles : num_sms);
   return launch_k(route_tc_kernel<TOK>, dim3(grid), dim3(kRcThreads), Cfg::kSmemBytes, st,
-                  false, tmR, tmH, bias, T, H, E, top_k, renorm, ids, w, zero_buf, zero_count,
-                  err);
+                  after_prev, tmR, tmH, bias, T, H, E, top_k, renorm, ids, w, zero_buf,
+                  zero_count, err);
 }
 
 }  // namespace
@@ -419,17 +420,17 @@ bool route_uses_tensor_cores(int T, int E) { return T > 2048 && E <= 128; }
 cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                             int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                             float* topk_w, float* zero_buf, long long zero_count, int num_sms,
-                            unsigned* err, cudaStream_t st) {
+                            unsigned* err, bool after_prev, cudaStream_t st) {
   // The smallest token tile that leaves at most one tile per SM (a CTA's time
   // is mostly its pass over the router matrix); beyond, 128-token tiles.
   if ((T + 31) / 32 <= num_sms)
     return launch_tok<32>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, num_sms, err, st);
+                          zero_buf, zero_count, num_sms, err, after_prev, st);
   if ((T + 63) / 64 <= num_sms)
     return launch_tok<64>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, num_sms, err, st);
+                          zero_buf, zero_count, num_sms, err, after_prev, st);
   return launch_tok<128>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, num_sms, err, st);
+                         zero_buf, zero_count, num_sms, err, after_prev, st);
 }
 
 }  // namespace mm

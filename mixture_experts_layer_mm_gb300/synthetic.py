@@ -137,3 +137,21 @@ def random_small_inputs(seed: int, T: int, H: int, E: int, I: int,
     if bias:
         d["router_bias"] = rng.standard_normal(E, dtype=np.float32)
     return d
+
+
+def make_norm_inputs(seed: int, T: int, H: int, residual_std: float = 2.0) -> dict:
+    """Inputs of the add + RMSNorm step before the layer (stream (seed, 4)):
+    x (the attention output) ~ N(0, 1), residual ~ N(0, residual_std^2) and
+    the norm weight 1 + N(0, 0.25^2), all rounded once to bf16."""
+    rng = np.random.default_rng((seed, 4))
+    return {"x": _normal_bf16(rng, (T, H), 1.0),
+            "residual": _normal_bf16(rng, (T, H), residual_std),
+            "norm_w": f32_to_bf16_bits(1.0 + 0.25 * rng.standard_normal(H, dtype=np.float32))}
+
+
+def make_dense_weights(seed: int, H: int, I: int, std: float = 0.02) -> dict:
+    """Weights of a dense gated MLP (stream (seed, 5)): w_gate_up [2I, H]
+    (gate rows first) and w_down [H, I], N(0, std^2) rounded to bf16."""
+    rng = np.random.default_rng((seed, 5))
+    return {"w_gate_up": _normal_bf16(rng, (2 * I, H), std),
+            "w_down": _normal_bf16(rng, (H, I), std)}

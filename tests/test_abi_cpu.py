@@ -97,6 +97,27 @@ def test_gated_mlp_host_checks(lib):
     assert mm.mm_gated_mlp_workspace_size(8, 128, 64) > 0
 
 
+def test_add_norm_host_checks(lib):
+    import ctypes
+    L = mm.lib()
+    f = ctypes.c_float
+    # add + RMSNorm alone: nulls, H % 64, negative or NaN eps, misaligned, T == 0
+    assert L.mm_add_rmsnorm(None, None, None, f(1e-6), 4, 64, None, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_add_rmsnorm(16, None, 16, f(1e-6), 4, 96, 16, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_add_rmsnorm(16, None, 16, f(-1.0), 4, 64, 16, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_add_rmsnorm(16, None, 16, f(float("nan")), 4, 64, 16, None) == \
+        mm.MM_ERR_INVALID_ARG
+    assert L.mm_add_rmsnorm(16, 8, 16, f(1e-6), 4, 64, 16, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_add_rmsnorm(None, None, None, f(1e-6), 0, 64, None, None) == mm.MM_OK
+    # the layer behind it: null norm weight, bad shape, T == 0
+    assert L.mm_moe_forward_add_norm(16, None, None, f(1e-6), 16, 16, 16, 4, 64, 8, 64, 2, 1, 16,
+                                     None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_moe_forward_add_norm(16, None, 16, f(1e-6), 16, 16, 16, 4, 64, 8, 96, 2, 1, 16,
+                                     None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_moe_forward_add_norm(None, None, None, f(1e-6), None, None, None, 0, 64, 8, 64, 2,
+                                     1, None, None) == mm.MM_OK
+
+
 def test_binding_raises_without_library(monkeypatch, tmp_path):
     import mixture_experts_layer_mm_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)
