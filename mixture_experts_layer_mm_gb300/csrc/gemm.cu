@@ -35,6 +35,7 @@
 // down multiplies by the routing weight and adds into the fp32 output
 // accumulator ("mini-sglang guide, chapter 7": expert outputs weighted by the
 // softmax scores and summed).
+#include <algorithm>
 #include <mutex>
 
 #include "mm.h"
@@ -60,13 +61,21 @@ struct GemmArgs {
   unsigned* err;
   int E, N, K, Tk, top_k;
   int n_mtiles;  // m-tiles per token chunk
+  int ksplit;    // K slices per (chunk, m-tile) (down mode only; 1 for gate_up)
   int w_rows;    // weight rows per expert in the 2-D weight view
   int m_step;    // weight rows per m-tile
   int a1_off;    // row offset of the A1 tile relative to A0
   int w_evict_first;  // weights are read by one token chunk only: stream them past L2
   int b_mode;         // how token rows reach shared memory (kB*)
   const uint16_t* hidden;  // kBLsuGather: token rows are read from here
+  const uint16_t* w;       // the weights (the L2 prefetch below)
+  int prefetch_guess;      // prefetch the guessed first tile's A0 rows into L2
 };
+
+// L2 prefetch of `bytes` (a multiple of 16) contiguous bytes from global memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // Token-row (B) paths.
 constexpr int kBTma = 0;        // 2-D TMA boxes of rows already in segment order
@@ -135,6 +144,16 @@ __device__ __forceinline__ void decode_tile(int tile, int n_mtiles, int E, const
   nrows = min(BN, off[e + 1] - row0);
 }
 
+// Tile index -> (expert, m-tile, first row, rows, K slice): tile =
+// (chunk * n_mtiles + m) * ksplit + slice.
+template <int BN>
+__device__ __forceinline__ void decode_tile_k(int tile, const GemmArgs& a, int E, const int* cs,
+                                              const int* off, int& e, int& m, int& row0,
+                                              int& nrows, int& slice) {
+  slice = tile % a.ksplit;
+  decode_tile<BN>(tile / a.ksplit, a.n_mtiles, E, cs, off, e, m, row0, nrows);
+}
+
 __device__ __forceinline__ bool aborted(const int* flag) {
   return *reinterpret_cast<const volatile int*>(flag) != 0;
 }
@@ -158,6 +177,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E;
+  // While the kernels before this one still run (the router at decode), start
+  // the weight stream: with about one chunk per selected expert and nearly
+  // all experts selected, this CTA's first tile is most likely (expert
+  // blockIdx / n_mtiles, m-tile blockIdx % n_mtiles). Its A0 rows (contiguous
+  // in memory) are prefetched into L2; a wrong guess only costs bandwidth.
+  if (a.prefetch_guess && tid == 0) {
+    const int ge = (int)blockIdx.x / a.n_mtiles, gm = (int)blockIdx.x % a.n_mtiles;
+    if (ge < E) {
+      const long long row = (long long)ge * a.w_rows + (long long)gm * a.m_step;
+      const uint32_t bytes = (uint32_t)kGM * (uint32_t)a.K * 2u;
+      const char* base = reinterpret_cast<const char*>(a.w + row * a.K);
+      for (uint32_t off = 0; off < bytes; off += 65536u)
+        prefetch_l2_bulk(base + off, bytes - off < 65536u ? bytes - off : 65536u);
+    }
+  }
   pdl_wait();  // the grouping and the token rows come from the kernels before
   pdl_trigger();
 
@@ -188,7 +222,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 31) cs_s[E] = incl;
   }
   __syncthreads();
-  const int total_tiles = cs_s[E] * a.n_mtiles;
+  const int total_tiles = cs_s[E] * a.n_mtiles * a.ksplit;
   if ((int)blockIdx.x >= total_tiles) return;  // uniform across the CTA
 
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -226,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_s;
-  const int nk = a.K / KB;
+  const int nk = a.K / KB / a.ksplit;  // K steps per tile (its slice of K)
 
   if (warp == 0) {
     // --------------------------------------------- weight (A) TMA producer ---
@@ -236,12 +270,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t ph = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         if (aborted(&abort_s)) break;
-        int e, m, row0, nrows;
-        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
         const int wrow0 = e * a.w_rows + m * a.m_step;
         const int wrow1 = wrow0 + a.a1_off;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
           if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
             signal_abort(&abort_s, a.err);
             ok = false;
@@ -281,8 +315,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint16_t* src[kPasses];
       const uint16_t* nxt[kPasses];
       auto fetch_rows = [&](int tl, const uint16_t* (&rows)[kPasses]) {
-        int e, m, row0, nrows;
-        if (tl < total_tiles) decode_tile<BN>(tl, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
 #pragma unroll
         for (int p = 0; p < kPasses; ++p) {
           const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
@@ -297,7 +331,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
         for (int p = 0; p < kPasses; ++p) src[p] = nxt[p];
         fetch_rows(tile + gridDim.x, nxt);
-        for (int kb = 0; kb < nk; ++kb) {
+        const int slice = tile % a.ksplit;
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
           if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
@@ -329,8 +364,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // next tile are fetched one tile ahead so their latency is hidden.
       int nxt[4];
       auto fetch_rows = [&](int tl, int (&rows)[4]) {
-        int e, m, row0, nrows;
-        if (tl < total_tiles) decode_tile<BN>(tl, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = 4 * lane + j;
@@ -343,12 +378,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (aborted(&abort_s)) break;
         int rows[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
         fetch_rows(tile + gridDim.x, nxt);
-        int e, m, row0, nrows;
-        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
         const int n_g4 = ((nrows + 15) & ~15) / 4;  // rows the MMA reads, 4 per gather
         const uint32_t bytes = n_g4 * 4 * Cfg::kRowBytes;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
           if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) {
@@ -372,10 +407,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (lane == 0) {
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
         if (aborted(&abort_s)) break;
-        int e, m, row0, nrows;
-        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
           if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
             signal_abort(&abort_s, a.err);
             ok = false;
@@ -401,8 +436,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int it = 0;
       for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
         if (aborted(&abort_s)) break;
-        int e, m, row0, nrows;
-        decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+        int e, m, row0, nrows, slice;
+        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
         const int b = it % NACC;
         const uint32_t use = static_cast<uint32_t>(it / NACC);
         if (!mbar_wait(smem_u32(&tempty[b]), (use & 1u) ^ 1u)) {
@@ -415,7 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(b * 2 * BN);
         const uint32_t d1 = d0 + BN;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
           if (!mbar_wait(smem_u32(&full[s]), ph)) {
             signal_abort(&abort_s, a.err);
             ok = false;
@@ -430,7 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t da0 = sdesc_kmajor<Cfg::kRowBytes>(st + kk * 32);
             const uint64_t da1 = sdesc_kmajor<Cfg::kRowBytes>(st + Cfg::kABytes + kk * 32);
             const uint64_t db = sdesc_kmajor<Cfg::kRowBytes>(st + 2 * Cfg::kABytes + kk * 32);
-            const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+            const uint32_t acc = (kb != slice * nk || kk != 0) ? 1u : 0u;
             umma_bf16(d0, da0, db, idesc, acc);
             umma_bf16(d1, da1, db, idesc, acc);
           }
@@ -456,8 +491,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int it = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
       if (aborted(&abort_s)) break;
-      int e, m, row0, nrows;
-      decode_tile<BN>(tile, a.n_mtiles, E, cs_s, off_s, e, m, row0, nrows);
+      int e, m, row0, nrows, slice;
+      decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
       const int b = it % NACC;
       const uint32_t use = static_cast<uint32_t>(it / NACC);
       // Down mode: lane j holds the slot id and routing weight of column j of
@@ -632,6 +667,16 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   // token chunks read each weight tile: keep the weights at normal priority.
   a.w_evict_first = (long long)T * top_k <= (long long)E * (BN / 2) ? 1 : 0;
   a.hidden = x_is_hidden ? X : nullptr;
+  a.w = W;
+  // Decode-sized gate_up (rows gathered from hidden) with enough assignments
+  // that nearly every expert is selected (T*k >= 4E: 98 % expected under
+  // uniform routing), where the guess of the first tile holds: overlap the
+  // router with the first tile's weight stream. With few selected experts
+  // (a skewed or tiny batch) the guess is mostly wrong and only costs
+  // bandwidth (T=1: 60 -> 63 us), so it is not made.
+  a.prefetch_guess = (MODE == MM_GEMM_GATE_UP && x_is_hidden &&
+                      gate_up_gathers_rows(T, top_k, E) && (long long)T * top_k >= 4LL * E)
+                         ? 1 : 0;
   if (MODE == MM_GEMM_GATE_UP && x_is_hidden)
     a.b_mode = gate_up_gathers_rows(T, top_k, E) ? kBTmaGather : kBLsuGather;
   else
@@ -647,6 +692,22 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
     a.a1_off = kGM;
     a.n_mtiles = (N + 2 * kGM - 1) / (2 * kGM);
   }
+  // Down mode with too few (chunk, m-tile) pairs to fill the SMs (small
+  // batches, the dense MLP at decode): split K into slices whose partial sums
+  // the epilogue adds into the fp32 accumulator like any other contribution
+  // (so the order of the additions, and the last bits of out, may vary from
+  // call to call). There are at most min(E, T*k) + T*k/BN chunks.
+  a.ksplit = 1;
+  if (MODE == MM_GEMM_DOWN) {
+    const long long rows = (long long)T * top_k;
+    const long long tiles = (std::min<long long>(E, rows) + rows / BN) * a.n_mtiles;
+    const int nkb = K / KB;
+    for (int d = nkb / 2; d >= 2; --d)  // at least two K steps per slice
+      if (nkb % d == 0 && tiles * d <= num_sms) {
+        a.ksplit = d;
+        break;
+      }
+  }
   CUtensorMap tmW, tmX;
   if (!make_tensor_map_2d(&tmW, W, (uint64_t)E * a.w_rows, (uint64_t)K, kGM, KB))
     return cudaErrorInvalidValue;
@@ -658,7 +719,7 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
                         ? make_tensor_map_2d(&tmX, X, (uint64_t)x_rows, (uint64_t)K, BN, KB)
                         : make_tensor_map_2d(&tmX, X, (uint64_t)T, (uint64_t)K, 1, KB);
   if (!ok_x) return cudaErrorInvalidValue;
-  const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles;
+  const long long max_tiles = (capacity / BN + E) * (long long)a.n_mtiles * a.ksplit;
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
   return launch_k(grouped_gemm_kernel<MODE, BN, S, NACC, KB>, dim3(grid), dim3(kGemmThreads),
                   Cfg::kSmemBytes, st, after_prev, tmW, tmX, a);

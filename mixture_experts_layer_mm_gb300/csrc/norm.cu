@@ -56,6 +56,8 @@ __device__ __forceinline__ uint32_t norm_pair(uint32_t r, uint32_t w, float inv)
   return pack_bf16(__fmul_rn(bf16_lo(w), ylo), __fmul_rn(bf16_hi(w), yhi));
 }
 
+constexpr int kNormBatch = 8;  // chunks a lane has in flight at once
+
 __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const uint4* __restrict__ x,
                                                           uint4* __restrict__ residual,
                                                           const uint4* __restrict__ weight,
@@ -64,34 +66,58 @@ __global__ void __launch_bounds__(256) add_rmsnorm_kernel(const uint4* __restric
   pdl_wait();  // x may come from the kernel before this one on the stream
   pdl_trigger();
   const int lane = threadIdx.x & 31;
-  const int h8 = H / 8;  // chunks per row
+  const int h8 = H / 8;                 // chunks per row
+  const int per = (h8 - lane + 31) / 32;  // this lane's chunks: lane, lane + 32, ...
   const int warps = gridDim.x * (blockDim.x >> 5);
   for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
-    const uint4* xr = x + (size_t)t * h8;
-    uint4* rr = residual != nullptr ? residual + (size_t)t * h8 : nullptr;
+    const uint4* xr = x + (size_t)t * h8 + lane;
+    uint4* rr = residual != nullptr ? residual + (size_t)t * h8 + lane : nullptr;
     float acc = 0.f;
-    for (int c = lane; c < h8; c += 32) {
-      uint4 r = __ldg(xr + c);
-      if (rr != nullptr) {
-        r = add_chunk(r, rr[c]);
-        rr[c] = r;  // residual' in place
-      }
-      acc = chunk_sumsq(acc, r);
+    // Pass 1, kNormBatch chunks at a time: all loads of a batch are issued
+    // before any of them is used; the squares are added in chunk order.
+    for (int b0 = 0; b0 < per; b0 += kNormBatch) {
+      uint4 r[kNormBatch], q[kNormBatch];
+#pragma unroll
+      for (int i = 0; i < kNormBatch; ++i)
+        if (b0 + i < per) {
+          r[i] = __ldg(xr + 32 * (b0 + i));
+          if (rr != nullptr) q[i] = rr[32 * (b0 + i)];
+        }
+#pragma unroll
+      for (int i = 0; i < kNormBatch; ++i)
+        if (b0 + i < per) {
+          if (rr != nullptr) {
+            r[i] = add_chunk(r[i], q[i]);
+            rr[32 * (b0 + i)] = r[i];  // residual' in place
+          }
+          acc = chunk_sumsq(acc, r[i]);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
     const float mean = __fdiv_rn(acc, (float)H);
     const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-    uint4* nr = normed + (size_t)t * h8;
-    for (int c = lane; c < h8; c += 32) {
-      const uint4 r = rr != nullptr ? rr[c] : __ldg(xr + c);  // this thread's own writes
-      const uint4 w = __ldg(weight + c);
-      uint4 o;
-      o.x = norm_pair(r.x, w.x, inv);
-      o.y = norm_pair(r.y, w.y, inv);
-      o.z = norm_pair(r.z, w.z, inv);
-      o.w = norm_pair(r.w, w.w, inv);
-      nr[c] = o;
+    uint4* nr = normed + (size_t)t * h8 + lane;
+    const uint4* wr = weight + lane;
+    for (int b0 = 0; b0 < per; b0 += kNormBatch) {
+      uint4 r[kNormBatch], w[kNormBatch];
+#pragma unroll
+      for (int i = 0; i < kNormBatch; ++i)
+        if (b0 + i < per) {
+          // residual' as this thread wrote it, or x itself
+          r[i] = rr != nullptr ? rr[32 * (b0 + i)] : __ldg(xr + 32 * (b0 + i));
+          w[i] = __ldg(wr + 32 * (b0 + i));
+        }
+#pragma unroll
+      for (int i = 0; i < kNormBatch; ++i)
+        if (b0 + i < per) {
+          uint4 o;
+          o.x = norm_pair(r[i].x, w[i].x, inv);
+          o.y = norm_pair(r[i].y, w[i].y, inv);
+          o.z = norm_pair(r[i].z, w[i].z, inv);
+          o.w = norm_pair(r[i].w, w[i].w, inv);
+          nr[32 * (b0 + i)] = o;
+        }
     }
   }
 }

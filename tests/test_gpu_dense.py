@@ -1,8 +1,9 @@
 """mm_gated_mlp: the dense SwiGLU MLP ("模型与权重加载", GatedMLP) through the
 grouped-GEMM kernels, against the oracle's expert loop with one expert,
 top_k = 1 and weight 1 (which the oracle's pins tie to the textbook dense
-MLP). With a single contribution per output element the result is
-deterministic, so two calls must agree bit for bit."""
+MLP). When the down GEMM splits K (few tiles for the SMs), its partial sums
+reach the fp32 accumulator in no fixed order, so each call is checked
+against the oracle on its own."""
 import numpy as np
 import pytest
 import torch
@@ -29,11 +30,11 @@ def test_gated_mlp(T, H, I):
     out2 = mm.mm_gated_mlp(dev_bf16(d["hidden"]), dev_bf16(wgu), dev_bf16(wd))
     torch.cuda.synchronize()
     assert mm.mm_poll_device_status() == mm.MM_OK
-    assert torch.equal(out, out2)
     ids = np.zeros((T, 1), dtype=np.int32)
     w = np.ones((T, 1), dtype=np.float32)
     ref = O.experts_loop(d["hidden"], d["w_gate_up"], d["w_down"], ids, w)
     assert_out_close(out.float().cpu().numpy(), ref, "dense GatedMLP")
+    assert_out_close(out2.float().cpu().numpy(), ref, "dense GatedMLP, second call")
 
 
 def test_gated_mlp_args():
