@@ -12,9 +12,12 @@
 // Each block first copies its tokens' ids to shared memory (one coalesced
 // pass), then works from there.
 // Small batches (T <= 1024 and T*k <= 8192): one block does histogram, scan
-// and scatter in a single launch. Otherwise: two launches over blocks of 256
+// and scatter in a single launch (for T <= 64 with per-expert 64-bit token
+// masks instead of ballots: align_tiny, which the router also runs). Otherwise: two launches over blocks of 256
 // tokens (per-block counts; then each block derives its own slot bases from
 // all blocks' counts and scatters); no block ever waits on another.
+#include <algorithm>
+
 #include "align_block.cuh"
 
 namespace mm {
@@ -29,7 +32,10 @@ __global__ void __launch_bounds__(1024) align_single_kernel(
   extern __shared__ __align__(16) unsigned char smem[];
   pdl_wait();
   pdl_trigger();
-  align_one_block(ids, T, k, E, bm, capacity, sorted, offsets, counts, err, smem);
+  if (T <= kTinyMaxTokens)
+    align_tiny(ids, T, k, E, bm, capacity, sorted, offsets, counts, err, smem);
+  else
+    align_one_block(ids, T, k, E, bm, capacity, sorted, offsets, counts, err, smem);
 }
 
 __global__ void __launch_bounds__(kAlignBlockTokens) align_count_kernel(
@@ -167,8 +173,12 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
     attr_done[dev] = true;
   }
   if (align_single_block(T, top_k)) {
-    const int nwarps = T <= 32 ? 1 : (T + 31) / 32;
-    const size_t smem = align_smem_bytes(nwarps, E, top_k);
+    // T <= 64: the bitmask grouping, with 8 warps; else one warp per 32 tokens.
+    const int nwarps = T <= kTinyMaxTokens ? 8 : (T + 31) / 32;
+    const size_t smem = T <= kTinyMaxTokens
+                            ? std::max(align_tiny_smem_bytes(E, T * top_k),
+                                       align_smem_bytes(nwarps, E, top_k))
+                            : align_smem_bytes(nwarps, E, top_k);
     return launch_k(align_single_kernel, dim3(1), dim3(nwarps * 32), smem, st, after_prev,
                     topk_ids, T, top_k, E, block_m, capacity, sorted, offsets, counts, err);
   }

@@ -180,5 +180,98 @@ __device__ __forceinline__ void align_one_block(const int32_t* __restrict__ ids,
   fill_padding(S.off, S.tot, E, capacity, T * k, sorted);
 }
 
+// The whole grouping for T <= 64 tokens (ids in global memory), by one block
+// of at least 32 threads, with the same output, the same drop rules (ids out
+// of range and repeats within a token, the later repeat, are dropped and
+// flagged) and the same stable order as align_one_block. A token set fits
+// in one 64-bit word: per expert, bit t is set when token t selected it (one
+// shared-memory atomicOr per id), so a count is a popcount and the rank of
+// token t among the expert's tokens is the popcount of the bits below t. No
+// per-warp ballot loops: it runs in a few barrier-separated steps.
+constexpr int kTinyMaxTokens = 64;
+
+__host__ __device__ constexpr size_t align_tiny_smem_bytes(int E, int n_ids) {
+  return (size_t)E * 8 + (size_t)(E + 1) * 4 + (size_t)E * 4 + (size_t)n_ids * 4 + 32 * 4;
+}
+
+__device__ __forceinline__ void align_tiny(const int32_t* __restrict__ ids, int T, int k, int E,
+                                           int bm, long long capacity,
+                                           int32_t* __restrict__ sorted,
+                                           int32_t* __restrict__ offsets,
+                                           int32_t* __restrict__ counts, unsigned* err,
+                                           unsigned char* smem) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long* mask = reinterpret_cast<unsigned long long*>(smem);  // [E]
+  int* off = reinterpret_cast<int*>(mask + E);                            // [E + 1]
+  int* cnt = off + E + 1;                                                 // [E]
+  int* ids_s = cnt + E;                                                   // [T * k]
+  int* wsum = ids_s + T * k;                                              // [32]
+  const int n = T * k;
+  for (int e = tid; e < E; e += nt) mask[e] = 0ull;
+  for (int i = tid; i < n; i += nt) ids_s[i] = ids[i];
+  __syncthreads();
+  bool bad = false;
+  for (int i = tid; i < n; i += nt) {
+    const int t = i / k, id = ids_s[i];
+    bool drop = id < 0 || id >= E;
+    for (int jj = t * k; jj < i && !drop; ++jj) drop = ids_s[jj] == id;  // an earlier repeat
+    bad |= drop;
+    if (!drop) atomicOr(&mask[id], 1ull << t);
+  }
+  if (bad && err != nullptr) atomicOr(err, kDevErrBadIds);
+  __syncthreads();
+  // Exclusive scan of the block-padded counts over the experts (E <= 32 *
+  // warps * per-thread loop), one pass per group of nt experts.
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += nt) {
+    const int e = e0 + tid;
+    const int c = e < E ? __popcll(mask[e]) : 0;
+    const int v = (c + bm - 1) / bm * bm;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = (nt + 31) / 32;
+      int w = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, w, o);
+        if (lane >= o) w += u;
+      }
+      if (lane < nw) wsum[lane] = w;  // inclusive totals of the warps
+    }
+    __syncthreads();
+    const int before = carry + (warp > 0 ? wsum[warp - 1] : 0) + incl - v;
+    if (e < E) {
+      off[e] = before;
+      cnt[e] = c;
+    }
+    carry += wsum[(nt + 31) / 32 - 1];
+    __syncthreads();
+  }
+  if (tid == 0) off[E] = carry;
+  __syncthreads();
+  for (int e = tid; e <= E; e += nt) {
+    offsets[e] = off[e];
+    if (e < E && counts != nullptr) counts[e] = cnt[e];
+  }
+  for (int i = tid; i < n; i += nt) {
+    const int t = i / k, id = ids_s[i];
+    if (id < 0 || id >= E) continue;
+    const unsigned long long m = mask[id];
+    if (!((m >> t) & 1ull)) continue;
+    bool rep = false;
+    for (int jj = t * k; jj < i && !rep; ++jj) rep = ids_s[jj] == id;
+    if (rep) continue;
+    sorted[off[id] + __popcll(m & ((1ull << t) - 1ull))] = i;
+  }
+  fill_padding(off, cnt, E, capacity, n, sorted);
+}
+
 }  // namespace alignblk
 }  // namespace mm

@@ -291,7 +291,9 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   }
   const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
   const bool fused = route_fuses_align(T, top_k);
-  if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, acc, nacc, &fa,
+  // The accumulator is zeroed by the gate_up kernel (on every SM, while the
+  // router runs), not by the router.
+  if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, nullptr, 0, &fa,
                    s->sms, s->status, norm != nullptr, st) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
@@ -306,7 +308,7 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   if (!mark(2)) return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_GATE_UP, L.rows_in_order ? xs : hidden, !L.rows_in_order,
                           w_gate_up, act, sorted, offsets, nullptr, T, top_k, E, I, H, L.capacity,
-                          L.capacity, s->sms, s->status, true, st) != cudaSuccess ||
+                          L.capacity, s->sms, s->status, true, st, acc, nacc) != cudaSuccess ||
       !mark(3))
     return MM_ERR_CUDA;
   if (launch_grouped_gemm(MM_GEMM_DOWN, act, false, w_down, acc, sorted, offsets, w, T, top_k, E,

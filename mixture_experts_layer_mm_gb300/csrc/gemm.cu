@@ -70,6 +70,8 @@ struct GemmArgs {
   const uint16_t* hidden;  // kBLsuGather: token rows are read from here
   const uint16_t* w;       // the weights (the L2 prefetch below)
   int prefetch_guess;      // prefetch the guessed first tile's A0 rows into L2
+  float* zero_buf;         // gate_up: zero these floats first (the layer's accumulator)
+  long long zero_count;
 };
 
 // L2 prefetch of `bytes` (a multiple of 16) contiguous bytes from global memory.
@@ -191,6 +193,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (uint32_t off = 0; off < bytes; off += 65536u)
         prefetch_l2_bulk(base + off, bytes - off < 65536u ? bytes - off : 65536u);
     }
+  }
+  // The fp32 accumulator that the down GEMM of this call adds into is cleared
+  // here by every CTA, before the wait: the previous call's last reader of it
+  // (finalize) completed before this call's first kernel started, and the
+  // down GEMM starts only after this kernel has completed.
+  if (a.zero_buf != nullptr) {
+    float4* z = reinterpret_cast<float4*>(a.zero_buf);
+    const long long n4 = a.zero_count >> 2;
+    for (long long i = (long long)blockIdx.x * kGemmThreads + tid; i < n4;
+         i += (long long)gridDim.x * kGemmThreads)
+      z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   pdl_wait();  // the grouping and the token rows come from the kernels before
   pdl_trigger();
@@ -641,7 +654,8 @@ template <int MODE, int BN, int S, int NACC, int KB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
                        const int32_t* sorted, const int32_t* offsets, const float* topk_w, int T,
                        int top_k, int E, int N, int K, long long capacity, long long x_rows,
-                       int num_sms, unsigned* err, bool after_prev, cudaStream_t st) {
+                       int num_sms, unsigned* err, bool after_prev, cudaStream_t st,
+                       float* zero_buf, long long zero_count) {
   using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -668,6 +682,8 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   a.w_evict_first = (long long)T * top_k <= (long long)E * (BN / 2) ? 1 : 0;
   a.hidden = x_is_hidden ? X : nullptr;
   a.w = W;
+  a.zero_buf = zero_buf;
+  a.zero_count = zero_count;
   // Decode-sized gate_up (rows gathered from hidden) with enough assignments
   // that nearly every expert is selected (T*k >= 4E: 98 % expected under
   // uniform routing), where the guess of the first tile holds: overlap the
@@ -771,7 +787,8 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, long long x_rows, int num_sms, unsigned* err,
-                                bool after_prev, cudaStream_t st) {
+                                bool after_prev, cudaStream_t st, float* zero_buf,
+                                long long zero_count) {
   // 256x128 tiles with two accumulator sets: the epilogue of one tile overlaps
   // the main loop of the next. (256x256 tiles with one set measured slower at
   // every batch size: the epilogue no longer overlaps, and a segment just over
@@ -781,10 +798,11 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
   if (mode == MM_GEMM_GATE_UP)
     return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,
                                                       topk_w, T, top_k, E, N, K, capacity, x_rows,
-                                                      num_sms, err, after_prev, st);
+                                                      num_sms, err, after_prev, st, zero_buf,
+                                                      zero_count);
   return launch_cfg<MM_GEMM_DOWN, 128, 4, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T, top_k,
                                                  E, N, K, capacity, x_rows, num_sms, err,
-                                                 after_prev, st);
+                                                 after_prev, st, nullptr, 0);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,

@@ -113,11 +113,14 @@ bool gate_up_gathers_rows(int T, int top_k, int E);
 // x_is_hidden, else X = token rows already in segment order [x_rows, K]
 // (rows at or past x_rows read as zeros).
 // mode 1: X = act [x_rows, K], C = fp32 acc [T, N] += topk_w * (X W^T).
+// zero_buf (gate_up mode; may be NULL): zero_count floats the kernel zeroes
+// before it waits for the kernels before it (the layer's accumulator).
 cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, const uint16_t* W,
                                 void* C, const int32_t* sorted, const int32_t* offsets,
                                 const float* topk_w, int T, int top_k, int E, int N, int K,
                                 long long capacity, long long x_rows, int num_sms, unsigned* err,
-                                bool after_prev, cudaStream_t st);
+                                bool after_prev, cudaStream_t st, float* zero_buf = nullptr,
+                                long long zero_count = 0);
 
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
 // xs[r] = hidden[sorted[r] / top_k] (H bf16 per row) for r < offsets[E];

@@ -231,8 +231,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(
     else
       __syncthreads();
     if (rank == 0)
-      alignblk::align_one_block(ids_out, T, top_k, E, fa.block_m, fa.capacity, fa.sorted,
-                                fa.offsets, fa.counts, fa.err, smem);
+      alignblk::align_tiny(ids_out, T, top_k, E, fa.block_m, fa.capacity, fa.sorted,
+                           fa.offsets, fa.counts, fa.err, smem);
   }
 }
 
