@@ -508,7 +508,8 @@ def main():
     fused_align = shape.T <= 64 and shape.T * k <= 8192
     single_align = shape.T <= 1024 and shape.T * k <= 8192
     rows_gathered = shape.T * k > 64 * shape.E  # token rows copied into segment order
-    launches_per_step = (4 + (0 if fused_align else 1 if single_align else 2)
+    router_counts = shape.T > 2048 and shape.E <= 128  # the grouping is then one launch
+    launches_per_step = (4 + (0 if fused_align else 1 if (single_align or router_counts) else 2)
                          + (1 if rows_gathered else 0) + (1 if args.add_norm else 0))
     n_io = 2 if args.add_norm else 1  # x and residual in, out and residual back
 

@@ -63,10 +63,13 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_count_kernel(
 // padded offset plus the counts of all earlier blocks, summed here with
 // independent loads), then the stable scatter. Block 0 also writes the
 // offsets, the counts and the padding sentinels.
+// count_rows rows of per-expert counts, each over rows_per_block-th of a
+// block's tokens (1 for this file's count kernel; several for the
+// tensor-core router's smaller token tiles).
 __global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
-    const int32_t* __restrict__ ids, int T, int k, int E, int bm, long long capacity, int nblocks,
-    const int32_t* __restrict__ block_counts, int32_t* __restrict__ sorted,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ counts) {
+    const int32_t* __restrict__ ids, int T, int k, int E, int bm, long long capacity,
+    int count_rows, int rows_per_block, const int32_t* __restrict__ block_counts,
+    int32_t* __restrict__ sorted, int32_t* __restrict__ offsets, int32_t* __restrict__ counts) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr int W = kAlignBlockTokens / 32;
   const AlignSmem S = carve(smem, W, E);
@@ -75,12 +78,13 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
   pdl_wait();
   pdl_trigger();
   stage_ids(ids, T, k, tok0, S.ids);
+  const int first_row = (int)blockIdx.x * rows_per_block;  // this block's first count row
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int before = 0, total = 0;
 #pragma unroll 8
-    for (int b = 0; b < nblocks; ++b) {
+    for (int b = 0; b < count_rows; ++b) {
       const int c = __ldg(block_counts + (size_t)b * E + e);
-      before += b < (int)blockIdx.x ? c : 0;
+      before += b < first_row ? c : 0;
       total += c;
     }
     S.tot[e] = total;
@@ -189,7 +193,29 @@ cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int b
   if (e != cudaSuccess) return e;
   return launch_k(align_place_kernel, dim3(nblocks), dim3(kAlignBlockTokens),
                   smem + (size_t)E * 4, st, true, topk_ids, T, top_k, E, block_m, capacity,
-                  nblocks, static_cast<const int32_t*>(scratch), sorted, offsets, counts);
+                  nblocks, 1, static_cast<const int32_t*>(scratch), sorted, offsets, counts);
+}
+
+cudaError_t launch_align_from_counts(const int32_t* topk_ids, int T, int top_k, int E,
+                                     int block_m, long long capacity,
+                                     const int32_t* tile_counts, int tile_tokens, int32_t* sorted,
+                                     int32_t* offsets, int32_t* counts, bool after_prev,
+                                     cudaStream_t st) {
+  static bool attr_done[kMaxDevices] = {};
+  const int dev = current_device();
+  if (!attr_done[dev]) {
+    const int multi = (int)align_smem_bytes(kAlignBlockTokens / 32, kMaxExperts, kMaxTopK);
+    const cudaError_t e = cudaFuncSetAttribute(
+        align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, multi + kMaxExperts * 4);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const int nblocks = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
+  const int rows = (T + tile_tokens - 1) / tile_tokens;
+  const size_t smem = align_smem_bytes(kAlignBlockTokens / 32, E, top_k) + (size_t)E * 4;
+  return launch_k(align_place_kernel, dim3(nblocks), dim3(kAlignBlockTokens), smem, st,
+                  after_prev, topk_ids, T, top_k, E, block_m, capacity, rows,
+                  kAlignBlockTokens / tile_tokens, tile_counts, sorted, offsets, counts);
 }
 
 }  // namespace mm

@@ -2,6 +2,7 @@
 // (SM count, status word, internal workspace) and the launch sequence of the
 // MoE layer. Every computing step runs in the kernels of route.cu, align.cu
 // and gemm.cu; this file only validates, lays out memory and launches.
+#include <algorithm>
 #include <mutex>
 
 #include "mm.h"
@@ -106,7 +107,12 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows
   L.sorted = take((size_t)L.capacity * 4);
   L.offsets = take((size_t)(E + 1) * 4);
   L.counts = take((size_t)E * 4);
-  L.scratch = take((size_t)align_scratch_ints(T, E, k) * 4);
+  // Align block counts, or the tensor-core router's per-tile counts (tiles of
+  // at least 32 tokens).
+  long long scratch_ints = align_scratch_ints(T, E, k);
+  if (route_uses_tensor_cores(T, E))
+    scratch_ints = std::max(scratch_ints, ((long long)T / 32 + 1) * E);
+  L.scratch = take((size_t)scratch_ints * 4);
   // Many rows per expert: gate_up reads its token rows as 2-D TMA boxes of a
   // copy in segment order (faster than gathering them inside the GEMM).
   L.rows_in_order = gather_rows && !gate_up_gathers_rows(T, k, E);
@@ -293,13 +299,23 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   const bool fused = route_fuses_align(T, top_k);
   // The accumulator is zeroed by the gate_up kernel (on every SM, while the
   // router runs), not by the router.
+  // The tensor-core router also counts each tile's experts, which leaves the
+  // grouping one launch.
+  const bool router_counts = route_uses_tensor_cores(T, E);
   if (launch_route(hidden, router_w, router_bias, T, H, E, top_k, renorm, ids, w, nullptr, 0, &fa,
-                   s->sms, s->status, norm != nullptr, st) != cudaSuccess ||
+                   s->sms, s->status, norm != nullptr, st,
+                   router_counts ? scratch : nullptr) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
-  if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets, counts,
-                             scratch, s->status, true, st) != cudaSuccess)
+  if (router_counts) {
+    if (launch_align_from_counts(ids, T, top_k, E, kForwardBlockM, L.capacity, scratch,
+                                 route_tc_tile_tokens(T, s->sms), sorted, offsets, counts, true,
+                                 st) != cudaSuccess)
+      return MM_ERR_CUDA;
+  } else if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets,
+                                    counts, scratch, s->status, true, st) != cudaSuccess) {
     return MM_ERR_CUDA;
+  }
   uint16_t* xs = at<uint16_t>(ws, L.xs);
   if (L.rows_in_order &&
       launch_gather_rows(hidden, sorted, offsets, T, top_k, E, H, xs, s->sms, true, st) !=

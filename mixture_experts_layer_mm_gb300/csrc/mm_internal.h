@@ -75,15 +75,28 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
                          const AlignOut* fuse_align, int num_sms, unsigned* err,
-                         bool after_prev, cudaStream_t st);
+                         bool after_prev, cudaStream_t st, int32_t* tile_counts = nullptr);
 
 // Whether launch_route runs the tensor-core router (route_tc.cu) for this
-// batch, and that router's launcher (same arguments, no grouping).
+// batch, its token tile, and its launcher (same arguments, no grouping;
+// tile_counts, if not NULL, receives per-tile expert counts [tiles][E] for
+// launch_align_from_counts).
 bool route_uses_tensor_cores(int T, int E);
+int route_tc_tile_tokens(int T, int num_sms);
 cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                             int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
-                            float* topk_w, float* zero_buf, long long zero_count, int num_sms,
-                            unsigned* err, bool after_prev, cudaStream_t st);
+                            float* topk_w, float* zero_buf, long long zero_count,
+                            int32_t* tile_counts, int num_sms, unsigned* err, bool after_prev,
+                            cudaStream_t st);
+
+// The grouping from per-tile expert counts the tensor-core router wrote
+// (rows of tile_tokens tokens; tile_tokens divides kAlignBlockTokens): one
+// launch instead of launch_align's count + place.
+cudaError_t launch_align_from_counts(const int32_t* topk_ids, int T, int top_k, int E,
+                                     int block_m, long long capacity,
+                                     const int32_t* tile_counts, int tile_tokens, int32_t* sorted,
+                                     int32_t* offsets, int32_t* counts, bool after_prev,
+                                     cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);

@@ -290,11 +290,11 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
                          float* topk_w, float* zero_buf, long long zero_count,
                          const AlignOut* fuse_align, int num_sms, unsigned* err,
-                         bool after_prev, cudaStream_t st) {
+                         bool after_prev, cudaStream_t st, int32_t* tile_counts) {
   // More than one 64-token tile and at most 128 experts: the tcgen05 router.
   if (route_uses_tensor_cores(T, E))
     return launch_route_tc(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                           zero_buf, zero_count, num_sms, err, after_prev, st);
+                           zero_buf, zero_count, tile_counts, num_sms, err, after_prev, st);
   AlignOut fa = {};
   if (fuse_align != nullptr && route_fuses_align(T, top_k)) fa = *fuse_align;
   if (E <= 32)

@@ -87,12 +87,13 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
 // winning and equal logits going to the lower expert id (each round: a
 // tournament over adjacent pairs in registers, the left and lower id keeping
 // ties, then a butterfly over the group); ids written in ascending order;
-// weights p or p / sum(p) over the selected. All 32 lanes of the warp call
+// weights p or p / sum(p) over the selected; with cnt (shared, may be NULL)
+// each selected expert's count is incremented. All 32 lanes of the warp call
 // this (t < 0: no token).
 template <int P, int NJ>
 __device__ __forceinline__ void finish_group(const float* __restrict__ row, int E, int top_k,
                                              int renorm, int t, int32_t* __restrict__ ids_out,
-                                             float* __restrict__ w_out) {
+                                             float* __restrict__ w_out, int* cnt) {
   constexpr uint32_t kAll = 0xffffffffu;
   const int h = threadIdx.x & (P - 1);
   const int nj = t >= 0 ? (E - h + P - 1) / P : 0;  // experts P*j + h < E
@@ -186,6 +187,7 @@ __device__ __forceinline__ void finish_group(const float* __restrict__ row, int 
       const float p = expf(row[id] - m) / s;
       ids_out[(size_t)t * top_k + slot] = id;
       w_out[(size_t)t * top_k + slot] = renorm ? p / psel : p;
+      if (cnt != nullptr) atomicAdd(cnt + id, 1);
     }
 }
 
@@ -195,13 +197,14 @@ __global__ void __launch_bounds__(kRcThreads, 1)
                     const __grid_constant__ CUtensorMap tmH, const float* __restrict__ bias,
                     int T, int H, int E, int top_k, int renorm, int32_t* __restrict__ ids_out,
                     float* __restrict__ w_out, float* __restrict__ zero_buf, long long zero_count,
-                    unsigned* err) {
+                    int32_t* __restrict__ tile_counts, unsigned* err) {
   using Cfg = RcCfg<TOK>;
   constexpr int S = Cfg::kStages;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[2 * S + 7];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
+  __shared__ int cnt_s[2][128];  // per-expert counts of the tile (by tile parity)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tiles = (T + TOK - 1) / TOK;
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(kRcThreads, 1)
     tmem_alloc(smem_u32(&tmem_base_s), Cfg::kTmemCols);
     tmem_relinquish();
   }
+  if (tid < 256) cnt_s[tid >> 7][tid & 127] = 0;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -343,10 +347,16 @@ __global__ void __launch_bounds__(kRcThreads, 1)
         rc_abort(&abort_s, err);
         break;
       }
-      // The previous tile's logits have been read by every epilogue thread.
+      // The previous tile's logits have been read by every epilogue thread,
+      // and its counts are complete: write them out and clear that buffer.
       if (it > 0 && !mbar_wait(smem_u32(lfree), static_cast<uint32_t>((it - 1) & 1))) {
         rc_abort(&abort_s, err);
         break;
+      }
+      if (it > 0 && tile_counts != nullptr && et < E) {
+        int* c = cnt_s[(it - 1) & 1];
+        tile_counts[(size_t)(tile - (int)gridDim.x) * E + et] = c[et];
+        c[et] = 0;
       }
       tc_fence_after();
       const uint32_t tb =
@@ -370,9 +380,20 @@ __global__ void __launch_bounds__(kRcThreads, 1)
       {
         const int n = et / Cfg::kP;  // the token this thread helps finish
         finish_group<Cfg::kP, Cfg::kNJ>(logits + n * Cfg::kLd, E, top_k, renorm,
-                                        n < ntok ? t0 + n : -1, ids_out, w_out);
+                                        n < ntok ? t0 + n : -1, ids_out, w_out,
+                                        tile_counts != nullptr ? cnt_s[it & 1] : nullptr);
       }
       mbar_arrive(smem_u32(lfree));
+    }
+    // The last tile's counts.
+    if (it > 0 && tile_counts != nullptr && !rc_aborted(&abort_s)) {
+      if (mbar_wait(smem_u32(lfree), static_cast<uint32_t>((it - 1) & 1))) {
+        if (et < E)
+          tile_counts[(size_t)(blockIdx.x + (it - 1) * (int)gridDim.x) * E + et] =
+              cnt_s[(it - 1) & 1][et];
+      } else {
+        rc_abort(&abort_s, err);
+      }
     }
   }
 
@@ -387,8 +408,8 @@ __global__ void __launch_bounds__(kRcThreads, 1)
 template <int TOK>
 cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int T,
                        int H, int E, int top_k, int renorm, int32_t* ids, float* w,
-                       float* zero_buf, long long zero_count, int num_sms, unsigned* err,
-                       bool after_prev, cudaStream_t st) {
+                       float* zero_buf, long long zero_count, int32_t* tile_counts, int num_sms,
+                       unsigned* err, bool after_prev, cudaStream_t st) {
   using Cfg = RcCfg<TOK>;
   static bool attr_done[kMaxDevices] = {};
   const int dev = current_device();
@@ -407,7 +428,7 @@ cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const f
                                        : (tiles < num_sms ? tiles : num_sms);
   return launch_k(route_tc_kernel<TOK>, dim3(grid), dim3(kRcThreads), Cfg::kSmemBytes, st,
                   after_prev, tmR, tmH, bias, T, H, E, top_k, renorm, ids, w, zero_buf,
-                  zero_count, err);
+                  zero_count, tile_counts, err);
 }
 
 }  // namespace
@@ -417,20 +438,28 @@ cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const f
 // per tile (about 16 us, bound by one SM's load latency).
 bool route_uses_tensor_cores(int T, int E) { return T > 2048 && E <= 128; }
 
-cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
-                            int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
-                            float* topk_w, float* zero_buf, long long zero_count, int num_sms,
-                            unsigned* err, bool after_prev, cudaStream_t st) {
+int route_tc_tile_tokens(int T, int num_sms) {
   // The smallest token tile that leaves at most one tile per SM (a CTA's time
   // is mostly its pass over the router matrix); beyond, 128-token tiles.
-  if ((T + 31) / 32 <= num_sms)
+  if ((T + 31) / 32 <= num_sms) return 32;
+  if ((T + 63) / 64 <= num_sms) return 64;
+  return 128;
+}
+
+cudaError_t launch_route_tc(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                            int T, int H, int E, int top_k, int renorm, int32_t* topk_ids,
+                            float* topk_w, float* zero_buf, long long zero_count,
+                            int32_t* tile_counts, int num_sms, unsigned* err, bool after_prev,
+                            cudaStream_t st) {
+  const int tok = route_tc_tile_tokens(T, num_sms);
+  if (tok == 32)
     return launch_tok<32>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, num_sms, err, after_prev, st);
-  if ((T + 63) / 64 <= num_sms)
+                          zero_buf, zero_count, tile_counts, num_sms, err, after_prev, st);
+  if (tok == 64)
     return launch_tok<64>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                          zero_buf, zero_count, num_sms, err, after_prev, st);
+                          zero_buf, zero_count, tile_counts, num_sms, err, after_prev, st);
   return launch_tok<128>(hidden, router_w, bias, T, H, E, top_k, renorm, topk_ids, topk_w,
-                         zero_buf, zero_count, num_sms, err, after_prev, st);
+                         zero_buf, zero_count, tile_counts, num_sms, err, after_prev, st);
 }
 
 }  // namespace mm
