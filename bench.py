@@ -67,6 +67,39 @@ def dist_info():
     return ws, rank, local
 
 
+# Replicas: each rank runs the whole layer on its own batch (tokens are
+# independent units; the layer has no exchange step), so the only
+# cross-rank traffic is the barrier around the timed region and the maximum
+# of the per-rank times. These helpers work with the nccl (GPU) and gloo
+# (CPU) process groups alike.
+
+def replica_batch(shape, rank: int):
+    """The shape whose seeded hidden batch rank `rank` times. The weights are
+    drawn from the unmodified shape, so every replica holds the same layer."""
+    return synthetic.MoEShape(**{**shape.__dict__, "seed": rank})
+
+
+def barrier(ws: int) -> None:
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T: int, ws: int, ms: float) -> float:
+    """Whole-job throughput: the tokens of all replicas over the slowest
+    rank's time per step."""
+    return T * ws / (ms * 1e-3)
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons of one GPU, read through
     NVML every 10 ms on a background thread while the timed region runs.
@@ -340,7 +373,7 @@ def main():
         raise SystemExit("--add-norm takes no router bias (the Zipf sweep has one)")
     # Each replica gets its own batch (hidden seed = rank); the layer weights are shared.
     w = synthetic.make_weights(shape)
-    hid_np = synthetic.make_hidden(synthetic.MoEShape(**{**shape.__dict__, "seed": rank}))
+    hid_np = synthetic.make_hidden(replica_batch(shape, rank))
     bias_np = synthetic.make_router_bias(shape)
 
     def to_dev(bits):
@@ -366,18 +399,6 @@ def main():
             mm.mm_moe_forward_add_norm(x_d, nw_d, eps, router_w, w_gu, w_dn, k, renorm,
                                        residual=res_d, out=out)
 
-    def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     for _ in range(args.warmup):
         fwd()
@@ -390,7 +411,7 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         args.steps = int(min(5000, max(20, 600.0 / max(e0.elapsed_time(e1) / 5, 1e-3))))
-        args.steps = int(max_over_ranks(float(args.steps)))
+        args.steps = int(max_over_ranks(float(args.steps), ws, dev))
     st = mm.mm_poll_device_status()
     if st != mm.MM_OK:
         raise RuntimeError(f"device status after warm-up: {mm.status_string(st)}")
@@ -404,7 +425,7 @@ def main():
     flush = work["layer"]["bytes"] < 2 * l2_bytes
     scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         if flush:
@@ -421,19 +442,19 @@ def main():
                 fwd()
             t_end.record(stream)
         torch.cuda.synchronize()
-    barrier()
+    barrier(ws)
     if flush:
         ms = sum(a.elapsed_time(b) for a, b in step_ev) / args.steps
     else:
         ms = t_start.elapsed_time(t_end) / args.steps
-    ms = max_over_ranks(ms)
+    ms = max_over_ranks(ms, ws, dev)
     clocks = clk.summary()
 
     # ---- timed region B: same steps, stage events recorded around each kernel
     nb = min(args.steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mm.PROFILE_STAGES) + 1)]
            for _ in range(nb)]
-    barrier()
+    barrier(ws)
     torch.cuda.synchronize()
     for i in range(nb):
         if flush:
@@ -441,7 +462,7 @@ def main():
         mm.mm_moe_forward_profiled(hidden, router_w, w_gu, w_dn, k, renorm, evs[i], out=out,
                                    router_bias=bias)
     torch.cuda.synchronize()
-    barrier()
+    barrier(ws)
     stage_ms = {}
     for j, name in enumerate(mm.PROFILE_STAGES):
         stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
@@ -456,7 +477,7 @@ def main():
         r_host = torch.empty_like(h_host, pin_memory=True)
         r_host.copy_(res_d.cpu())
         r_back = torch.empty_like(h_host, pin_memory=True)
-    barrier()
+    barrier(ws)
     torch.cuda.synchronize()
     e2e_total = 0.0
     t0 = time.perf_counter()
@@ -479,14 +500,14 @@ def main():
             e2e_total += time.perf_counter() - t0
     if not flush:
         e2e_total = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_total / args.steps)
+    e2e_s = max_over_ranks(e2e_total / args.steps, ws, dev)
     st = mm.mm_poll_device_status()
     if st != mm.MM_OK:
         raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
 
     pk, pk_kind = peaks()
     T_all = shape.T * ws
-    value = T_all / (ms * 1e-3)
+    value = job_tokens_per_s(shape.T, ws, ms)
     # The dominant kernel: the gate_up grouped GEMM (largest share of bytes and flops).
     dom = "gate_up"
     dom_ms = stage_ms[dom]
