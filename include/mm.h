@@ -267,6 +267,16 @@ int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,
  */
 int mm_poll_device_status(void* stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches one
+ * kernel whose mbarrier wait can never complete. Its bounded wait, the one
+ * every kernel of the library uses, gives up after about a second, records
+ * the timeout in the device status word and returns; the next
+ * mm_poll_device_status then reports MM_ERR_TIMEOUT (and clears the word).
+ * Nothing faults or hangs, and the context stays usable.
+ */
+int mm_selftest_wait_timeout(void* stream);
+
 /* Frees the internal workspaces of every device. Not thread-safe with calls in flight. */
 void mm_shutdown(void);
 

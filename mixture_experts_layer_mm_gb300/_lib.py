@@ -46,6 +46,7 @@ SIGNATURES = {
     "mm_moe_forward_add_norm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, _I, _I,
                                      _I, _P, _P]),
     "mm_poll_device_status": (_I, [_P]),
+    "mm_selftest_wait_timeout": (_I, [_P]),
     "mm_shutdown": (None, []),
 }
 
@@ -302,6 +303,11 @@ def mm_moe_forward_profiled(hidden, router_w, w_gate_up, w_down, top_k: int, ren
 def mm_poll_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(lib().mm_poll_device_status(_stream(stream)))
+
+
+def mm_selftest_wait_timeout(stream=None) -> None:
+    """Launches the kernel whose bounded wait must time out (see include/mm.h)."""
+    _check(lib().mm_selftest_wait_timeout(_stream(stream)), "mm_selftest_wait_timeout")
 
 
 def mm_shutdown() -> None:

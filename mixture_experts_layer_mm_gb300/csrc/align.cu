@@ -78,14 +78,32 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
   pdl_wait();
   pdl_trigger();
   stage_ids(ids, T, k, tok0, S.ids);
+  // Per expert, the counts of the rows before this block's first row and of
+  // all rows: G = blockDim / E threads per expert each sum every G-th row
+  // (partials parked in the ballot / prefix arrays, which are free until the
+  // scatter), then one thread per expert adds the G partials.
   const int first_row = (int)blockIdx.x * rows_per_block;  // this block's first count row
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  const int G = max(1, min((int)blockDim.x / E, W));  // the arrays hold W x E ints
+  int* part_before = S.pre;                               // [G][E]
+  int* part_total = reinterpret_cast<int*>(S.bal);        // [G][E]
+  for (int i = threadIdx.x; i < G * E; i += blockDim.x) {
+    const int e = i % E, g = i / E;
     int before = 0, total = 0;
 #pragma unroll 8
-    for (int b = 0; b < count_rows; ++b) {
+    for (int b = g; b < count_rows; b += G) {
       const int c = __ldg(block_counts + (size_t)b * E + e);
       before += b < first_row ? c : 0;
       total += c;
+    }
+    part_before[g * E + e] = before;
+    part_total[g * E + e] = total;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+    for (int g = 0; g < G; ++g) {
+      before += part_before[g * E + e];
+      total += part_total[g * E + e];
     }
     S.tot[e] = total;
     base_s[e] = before;
