@@ -539,8 +539,10 @@ def main():
     single_align = shape.T <= 1024 and shape.T * k <= 8192
     rows_gathered = shape.T * k > 64 * shape.E  # token rows copied into segment order
     router_counts = shape.T > 2048 and shape.E <= 128  # the grouping is then one launch
+    # with the router's counts and E % 4 == 0 the grouping also copies the rows
+    separate_copy = rows_gathered and not (router_counts and shape.E % 4 == 0)
     launches_per_step = (4 + (0 if fused_align else 1 if (single_align or router_counts) else 2)
-                         + (1 if rows_gathered else 0) + (1 if args.add_norm else 0))
+                         + (1 if separate_copy else 0) + (1 if args.add_norm else 0))
     n_io = 2 if args.add_norm else 1  # x and residual in, out and residual back
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,

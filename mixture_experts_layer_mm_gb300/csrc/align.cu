@@ -127,6 +127,152 @@ __global__ void __launch_bounds__(kAlignBlockTokens) align_place_kernel(
   block_scatter(S.ids, T, k, E, tok0, S.bal, S.pre, base_s, sorted);
 }
 
+// Counts of every expert before count row `first_row` and over all rows, from
+// rows of E ints: G = blockDim / (E/4) threads per column of 4 experts each
+// sum every G-th row with 16-byte loads, all of a thread's rows in flight
+// (partials parked in part_before / part_total, [G][E]); then one thread per
+// expert adds the G partials into before_s and tot_s. E % 4 == 0.
+__device__ __forceinline__ void count_prefix4(const int32_t* __restrict__ rows, int count_rows,
+                                              int E, int first_row, int gmax, int* part_before,
+                                              int* part_total, int* before_s, int* tot_s) {
+  const int E4 = E / 4;
+  const int G = max(1, min((int)blockDim.x / E4, gmax));
+  const int4* r4 = reinterpret_cast<const int4*>(rows);
+  for (int i = threadIdx.x; i < G * E4; i += blockDim.x) {
+    const int c = i % E4, g = i / E4;
+    int4 before = make_int4(0, 0, 0, 0), total = make_int4(0, 0, 0, 0);
+#pragma unroll 16
+    for (int b = g; b < count_rows; b += G) {
+      const int4 v = __ldg(r4 + (size_t)b * E4 + c);
+      total.x += v.x;
+      total.y += v.y;
+      total.z += v.z;
+      total.w += v.w;
+      if (b < first_row) {
+        before.x += v.x;
+        before.y += v.y;
+        before.z += v.z;
+        before.w += v.w;
+      }
+    }
+    *reinterpret_cast<int4*>(part_before + g * E + 4 * c) = before;
+    *reinterpret_cast<int4*>(part_total + g * E + 4 * c) = total;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+    for (int g = 0; g < G; ++g) {
+      before += part_before[g * E + e];
+      total += part_total[g * E + e];
+    }
+    tot_s[e] = total;
+    before_s[e] = before;
+  }
+}
+
+// The grouping and the token-row copy in one launch, from the per-tile
+// expert counts of the tensor-core router (count row c covers tokens
+// [c*R, (c+1)*R)). One CTA per count row: it derives its tile's slot bases
+// from all count rows, ranks its tokens by warp ballots, writes their slots
+// of sorted, then copies each token's row of hidden to the token's k slots
+// of xs (one read, k writes) and turns the padding rows of the experts
+// blockIdx.x, blockIdx.x + gridDim.x, ... into zeros. CTA 0 also writes the
+// offsets, the counts and the sentinels. Same output as align_place_kernel
+// followed by gather_rows_kernel. E % 4 == 0, R <= 32 * warps.
+constexpr int kPlaceRowsThreads = 512;
+
+struct PlaceRowsSmem {
+  uint32_t* bal;  // [W*E]
+  int* pre;       // [W*E]
+  int* tot;       // [E]   all tokens' counts
+  int* btot;      // [E]   this CTA's counts
+  int* off;       // [E+1]
+  int* base;      // [E]
+  int* ids;       // [R*k]
+  int* pos;       // [R*k]
+};
+
+__host__ __device__ constexpr size_t place_rows_smem_bytes(int W, int E, int R, int k) {
+  return (size_t)(2 * W * E + 4 * E + 1 + 2 * R * k) * 4;
+}
+
+__global__ void __launch_bounds__(kPlaceRowsThreads) align_place_rows_kernel(
+    const int32_t* __restrict__ ids, int T, int k, int E, int bm, long long capacity, int R,
+    int count_rows, const int32_t* __restrict__ tile_counts, const uint4* __restrict__ hidden,
+    int row16, int32_t* __restrict__ sorted, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ counts, uint4* __restrict__ xs) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int W = kPlaceRowsThreads / 32;
+  PlaceRowsSmem S;
+  S.bal = reinterpret_cast<uint32_t*>(smem);
+  S.pre = reinterpret_cast<int*>(S.bal + W * E);
+  S.tot = S.pre + W * E;
+  S.btot = S.tot + E;
+  S.off = S.btot + E;
+  S.base = S.off + E + 1;
+  S.ids = S.base + E;
+  S.pos = S.ids + R * k;
+  const int tok0 = blockIdx.x * R;
+  const int tend = min(T, tok0 + R);  // this CTA's tokens end here
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  stage_ids(ids, tend, k, tok0, S.ids);
+  count_prefix4(tile_counts, count_rows, E, blockIdx.x, W, S.pre,
+                reinterpret_cast<int*>(S.bal), S.base, S.tot);
+  __syncthreads();
+  if (threadIdx.x < 32) warp_scan_padded(S.tot, E, bm, S.off);
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+      offsets[e] = S.off[e];
+      if (e < E && counts != nullptr) counts[e] = S.tot[e];
+    }
+    fill_padding(S.off, S.tot, E, capacity, T * k, sorted);
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) S.base[e] += S.off[e];
+  // Bad ids were already flagged by the router.
+  block_ballots(S.ids, tend, k, E, tok0, S.bal, nullptr);
+  __syncthreads();
+  warp_prefix(S.bal, W, E, S.pre, S.btot);
+  __syncthreads();
+  block_scatter(S.ids, tend, k, E, tok0, S.bal, S.pre, S.base, sorted, S.pos);
+  __syncthreads();
+  // Token rows: warp w copies tokens w, w + W, ...; 8 x 16 bytes per lane in
+  // flight, each chunk stored to every slot of the token.
+  constexpr int kU = 8;
+  for (int tl = warp; tl < tend - tok0; tl += W) {
+    const uint4* src = hidden + (size_t)(tok0 + tl) * row16;
+    const int* pt = S.pos + tl * k;
+    for (int c0 = 0; c0 < row16; c0 += 32 * kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = c0 + u * 32 + lane;
+        if (i < row16) v[u] = __ldg(src + i);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int p = pt[j];
+        if (p < 0) continue;
+        uint4* dst = xs + (size_t)p * row16;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int i = c0 + u * 32 + lane;
+          if (i < row16) dst[i] = v[u];
+        }
+      }
+    }
+  }
+  // Padding rows of this CTA's experts (at most bm - 1 each).
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int r1 = S.off[e + 1];
+    for (int r = S.off[e] + S.tot[e] + warp; r < r1; r += W) {
+      uint4* dst = xs + (size_t)r * row16;
+      for (int i = lane; i < row16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
 // The grouping of a dense MLP: one expert holding every token in order
 // (sorted[r] = r, padding T up to a multiple of bm), routing weight 1, and
 // the fp32 output accumulator zeroed.
@@ -234,6 +380,31 @@ cudaError_t launch_align_from_counts(const int32_t* topk_ids, int T, int top_k, 
   return launch_k(align_place_kernel, dim3(nblocks), dim3(kAlignBlockTokens), smem, st,
                   after_prev, topk_ids, T, top_k, E, block_m, capacity, rows,
                   kAlignBlockTokens / tile_tokens, tile_counts, sorted, offsets, counts);
+}
+
+cudaError_t launch_align_place_rows(const int32_t* topk_ids, int T, int top_k, int E,
+                                    int block_m, long long capacity, const int32_t* tile_counts,
+                                    int tile_tokens, const uint16_t* hidden, int H, int32_t* sorted,
+                                    int32_t* offsets, int32_t* counts, uint16_t* xs,
+                                    bool after_prev, cudaStream_t st) {
+  if (E % 4 != 0 || tile_tokens > kPlaceRowsThreads || H % 8 != 0) return cudaErrorInvalidValue;
+  static bool attr_done[kMaxDevices] = {};
+  const int dev = current_device();
+  constexpr int W = kPlaceRowsThreads / 32;
+  if (!attr_done[dev]) {
+    const size_t most = place_rows_smem_bytes(W, kMaxExperts, 128, kMaxTopK);
+    const cudaError_t e = cudaFuncSetAttribute(
+        align_place_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  if (tile_tokens > 128) return cudaErrorInvalidValue;
+  const int rows = (T + tile_tokens - 1) / tile_tokens;
+  return launch_k(align_place_rows_kernel, dim3(rows), dim3(kPlaceRowsThreads),
+                  place_rows_smem_bytes(W, E, tile_tokens, top_k), st, after_prev, topk_ids, T,
+                  top_k, E, block_m, capacity, tile_tokens, rows, tile_counts,
+                  reinterpret_cast<const uint4*>(hidden), H / 8, sorted, offsets, counts,
+                  reinterpret_cast<uint4*>(xs));
 }
 
 }  // namespace mm

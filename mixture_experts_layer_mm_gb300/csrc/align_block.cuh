@@ -102,22 +102,27 @@ __device__ __forceinline__ void warp_scan_padded(const int* tot, int E, int bm, 
 }
 
 // Writes f = t*k + j of every valid, first-occurrence assignment of the
-// block's tokens at base[e] + pre_s + rank-in-warp.
+// block's tokens at base[e] + pre_s + rank-in-warp. With pos_s, also records
+// that slot at pos_s[tl*k + j] (-1 for a dropped id).
 __device__ __forceinline__ void block_scatter(const int* ids_s, int T, int k, int E, int tok0,
                                               const uint32_t* bal_s, const int* pre_s,
-                                              const int* base, int32_t* __restrict__ sorted) {
+                                              const int* base, int32_t* __restrict__ sorted,
+                                              int* pos_s = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tl = warp * 32 + lane, t = tok0 + tl;
   if (t >= T) return;
   const uint32_t lt = (1u << lane) - 1u;
   for (int j = 0; j < k; ++j) {
     const int id = ids_s[tl * k + j];
-    if (id < 0 || id >= E) continue;
-    bool dup = false;
-    for (int jj = 0; jj < j; ++jj) dup |= ids_s[tl * k + jj] == id;
-    if (dup) continue;
+    bool drop = id < 0 || id >= E;
+    for (int jj = 0; jj < j && !drop; ++jj) drop = ids_s[tl * k + jj] == id;
+    if (drop) {
+      if (pos_s != nullptr) pos_s[tl * k + j] = -1;
+      continue;
+    }
     const int pos = base[id] + pre_s[warp * E + id] + __popc(bal_s[warp * E + id] & lt);
     sorted[pos] = t * k + j;
+    if (pos_s != nullptr) pos_s[tl * k + j] = pos;
   }
 }
 

@@ -307,17 +307,25 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
                    router_counts ? scratch : nullptr) != cudaSuccess ||
       !mark(1))
     return MM_ERR_CUDA;
-  if (router_counts) {
+  uint16_t* xs = at<uint16_t>(ws, L.xs);
+  // With the router's counts and token rows wanted in segment order, the
+  // grouping and the row copy are one launch.
+  const int tile_tokens = router_counts ? route_tc_tile_tokens(T, s->sms) : 0;
+  const bool place_rows = router_counts && L.rows_in_order && E % 4 == 0 && tile_tokens <= 128;
+  if (place_rows) {
+    if (launch_align_place_rows(ids, T, top_k, E, kForwardBlockM, L.capacity, scratch,
+                                tile_tokens, hidden, H, sorted, offsets, counts, xs, true,
+                                st) != cudaSuccess)
+      return MM_ERR_CUDA;
+  } else if (router_counts) {
     if (launch_align_from_counts(ids, T, top_k, E, kForwardBlockM, L.capacity, scratch,
-                                 route_tc_tile_tokens(T, s->sms), sorted, offsets, counts, true,
-                                 st) != cudaSuccess)
+                                 tile_tokens, sorted, offsets, counts, true, st) != cudaSuccess)
       return MM_ERR_CUDA;
   } else if (!fused && launch_align(ids, T, top_k, E, kForwardBlockM, L.capacity, sorted, offsets,
                                     counts, scratch, s->status, true, st) != cudaSuccess) {
     return MM_ERR_CUDA;
   }
-  uint16_t* xs = at<uint16_t>(ws, L.xs);
-  if (L.rows_in_order &&
+  if (L.rows_in_order && !place_rows &&
       launch_gather_rows(hidden, sorted, offsets, T, top_k, E, H, xs, s->sms, true, st) !=
           cudaSuccess)
     return MM_ERR_CUDA;

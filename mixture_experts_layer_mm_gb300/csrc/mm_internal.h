@@ -97,6 +97,15 @@ cudaError_t launch_align_from_counts(const int32_t* topk_ids, int T, int top_k, 
                                      const int32_t* tile_counts, int tile_tokens, int32_t* sorted,
                                      int32_t* offsets, int32_t* counts, bool after_prev,
                                      cudaStream_t st);
+// launch_align_from_counts and launch_gather_rows in one launch (one CTA per
+// count row): the grouping, then xs[r] = hidden[sorted[r] / top_k] for the
+// segment rows and zeros for their padding. E % 4 == 0, tile_tokens <= 128,
+// H % 8 == 0 (else cudaErrorInvalidValue).
+cudaError_t launch_align_place_rows(const int32_t* topk_ids, int T, int top_k, int E,
+                                    int block_m, long long capacity, const int32_t* tile_counts,
+                                    int tile_tokens, const uint16_t* hidden, int H, int32_t* sorted,
+                                    int32_t* offsets, int32_t* counts, uint16_t* xs,
+                                    bool after_prev, cudaStream_t st);
 
 // Scratch ints the align launch needs (0 when one block covers all tokens).
 long long align_scratch_ints(int T, int E, int top_k);

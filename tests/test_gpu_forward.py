@@ -108,9 +108,11 @@ def test_forward_zipf_sweep(T):
     (300, 64, 256, 32, 64, False),
     (2000, 128, 16, 4, 320, True),
     # above 2048 tokens the tensor-core router also writes per-tile expert
-    # counts for the grouping: 32-, 64- and 128-token tiles
+    # counts for the grouping: 32-, 64- and 128-token tiles; with E % 4 == 0
+    # the grouping also copies the token rows (one launch), else a separate
+    # row copy follows it
     (3000, 64, 100, 8, 64, False), (5000, 128, 40, 5, 192, True),
-    (12000, 64, 128, 8, 64, True),
+    (12000, 64, 128, 8, 64, True), (2500, 64, 30, 4, 64, True),
 ])
 def test_forward_shapes(T, H, E, k, I, renorm):
     d = random_small_inputs(T + 3 * E, T, H, E, I, w_std=0.08, bias=(E % 2 == 0))
