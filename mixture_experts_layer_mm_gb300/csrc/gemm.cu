@@ -712,11 +712,14 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
   // batches, the dense MLP at decode): split K into slices whose partial sums
   // the epilogue adds into the fp32 accumulator like any other contribution
   // (so the order of the additions, and the last bits of out, may vary from
-  // call to call). There are at most min(E, T*k) + T*k/BN chunks.
+  // call to call). With n <= min(E, T*k) experts holding r_e >= 1 rows each,
+  // the chunks number sum ceil(r_e / BN) <= n + (T*k - n) / BN, which grows
+  // with n: at most min(E, T*k) + (T*k - min(E, T*k)) / BN.
   a.ksplit = 1;
   if (MODE == MM_GEMM_DOWN) {
     const long long rows = (long long)T * top_k;
-    const long long tiles = (std::min<long long>(E, rows) + rows / BN) * a.n_mtiles;
+    const long long busy = std::min<long long>(E, rows);
+    const long long tiles = (busy + (rows - busy) / BN) * a.n_mtiles;
     const int nkb = K / KB;
     for (int d = nkb / 2; d >= 2; --d)  // at least two K steps per slice
       if (nkb % d == 0 && tiles * d <= num_sms) {
@@ -795,6 +798,19 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
   // 256 rows adds a nearly empty chunk that re-reads the whole weight tile.)
   // (Stages of K = 32 with the 64-byte swizzle, 9 or 8 of them in the same
   // shared memory, measured slower than 4 stages of K = 64 at every size.)
+  // With few rows per expert (the decode regime, where gate_up gathers its
+  // rows from hidden) the token tile is at most 64 rows, and the 8 KB it
+  // frees per stage buys a fifth stage: more weight bytes in flight per SM.
+  if (gate_up_gathers_rows(T, top_k, E)) {
+    if (mode == MM_GEMM_GATE_UP)
+      return launch_cfg<MM_GEMM_GATE_UP, 64, 5, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,
+                                                       topk_w, T, top_k, E, N, K, capacity,
+                                                       x_rows, num_sms, err, after_prev, st,
+                                                       zero_buf, zero_count);
+    return launch_cfg<MM_GEMM_DOWN, 64, 5, 2, 64>(X, false, W, C, sorted, offsets, topk_w, T,
+                                                  top_k, E, N, K, capacity, x_rows, num_sms, err,
+                                                  after_prev, st, nullptr, 0);
+  }
   if (mode == MM_GEMM_GATE_UP)
     return launch_cfg<MM_GEMM_GATE_UP, 128, 4, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,
                                                       topk_w, T, top_k, E, N, K, capacity, x_rows,
