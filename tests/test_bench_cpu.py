@@ -1,0 +1,61 @@
+"""The arithmetic behind bench.py's roofline object, on CPU.
+
+The achieved bandwidth and flop rates divide algorithmic bytes and flops by
+measured times, so the counts themselves are checked here against values
+worked out by hand for the Qwen3-30B-A3B-shaped layer (H=2048, E=128, k=8,
+I=768): 6.29 MB of gate/up weights and 3.15 MB of down weights per selected
+expert, 76.0 MFLOP per token for the whole layer.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from mixture_experts_layer_mm_gb300 import synthetic as S  # noqa: E402
+
+
+def _all_experts_ids(T, k, E):
+    # token t takes experts t*k .. t*k+k-1 (mod E): with T*k >= E every expert appears
+    return (np.arange(T * k) % E).reshape(T, k).astype(np.int32)
+
+
+def test_decode_counts_by_hand():
+    sh = S.DECODE                              # T=64, H=2048, E=128, k=8, I=768
+    w = bench.algorithmic_work(sh, _all_experts_ids(sh.T, sh.top_k, sh.E))
+    assert w["D"] == 128
+    gate_up_weights = 128 * (2 * 768) * 2048 * 2          # 805,306,368 B
+    assert w["gate_up"]["bytes"] == gate_up_weights + 64 * 2048 * 2 + 512 * 768 * 2
+    assert w["gate_up"]["flops"] == 2 * 512 * 2048 * 1536  # 3.22 GFLOP
+    down_weights = 128 * 2048 * 768 * 2                   # 402,653,184 B
+    assert w["down"]["bytes"] == down_weights + 512 * 768 * 2 + 64 * 2048 * 4
+    assert w["down"]["flops"] == 2 * 512 * 768 * 2048
+    # per expert: 6.29 MB of gate/up rows, 3.15 MB of down rows
+    assert gate_up_weights / 128 == pytest.approx(6.29e6, rel=1e-3)
+    assert down_weights / 128 == pytest.approx(3.15e6, rel=2e-3)
+    # 76.0 MFLOP per token: router 2*E*H plus three expert projections per slot
+    assert w["layer"]["flops"] / sh.T == pytest.approx(76.02e6, rel=1e-4)
+    # the layer's bytes: every selected expert's three matrices, the router, x and out
+    assert w["layer"]["bytes"] == 128 * 3 * 2048 * 768 * 2 + 128 * 2048 * 2 + 2 * 64 * 2048 * 2
+
+
+def test_distinct_experts_follow_the_routing():
+    sh = S.DECODE
+    ids = np.tile(np.array([3, 9, 77, 3, 9, 77, 3, 9], dtype=np.int32), (sh.T, 1))
+    w = bench.algorithmic_work(sh, ids)
+    assert w["D"] == 3
+    assert w["gate_up"]["bytes"] == 3 * 1536 * 2048 * 2 + 64 * 2048 * 2 + 512 * 768 * 2
+
+
+def test_prefill_intensity_is_below_the_measured_ridge():
+    # 236 flop per algorithmic byte for gate_up at T=4096 (all experts selected),
+    # under the 1904.1 TF/s / 6783.5 GB/s = 281 flop/B ridge: reported as HBM-bound.
+    sh = S.PREFILL
+    w = bench.algorithmic_work(sh, _all_experts_ids(sh.T, sh.top_k, sh.E))
+    intensity = w["gate_up"]["flops"] / w["gate_up"]["bytes"]
+    assert intensity == pytest.approx(236.3, rel=1e-3)
+    assert intensity < 1904.1e12 / 6783.5e9
