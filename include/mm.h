@@ -213,8 +213,10 @@ int64_t mm_gated_mlp_workspace_size(int T, int H, int I);
 
 /*
  * The residual add + RMSNorm that precedes the MoE block in a decoder layer
- * ("mini-sglang guide": the decoder layer's post_attention_layernorm,
- * RMSNormFused, and the torch_ops rmsnorm / fused_add_rmsnorm listings):
+ * ("The op layer: BaseOP and the layers": the rmsnorm / fused_add_rmsnorm
+ * listings of "Ops: reference implementations and dispatch"; RMSNormFused and
+ * the post_attention_layernorm of DecoderLayer.forward in "RMSNorm and the
+ * residual"):
  *   residual' = bf16(x + residual)                  (written back to residual)
  *   normed    = bf16(norm_w * bf16(residual' * rsqrt(mean(residual'^2) + eps)))
  * With residual == NULL (the first layer) x is the residual and is only read.

@@ -1,6 +1,8 @@
 // The residual add + RMSNorm that precedes the MoE block of a decoder layer
-// ("mini-sglang guide": the decoder layer and RMSNormFused; the torch_ops
-// rmsnorm / fused_add_rmsnorm listings): residual' = bf16(x + residual),
+// ("The op layer: BaseOP and the layers": the rmsnorm / fused_add_rmsnorm
+// listings of "Ops: reference implementations and dispatch"; RMSNormFused
+// and DecoderLayer.forward of "RMSNorm and the residual"):
+// residual' = bf16(x + residual),
 // normed = bf16(weight * bf16(residual' * rsqrt(mean(residual'^2) + eps))).
 //
 // One warp per row, 16-byte accesses. Lane l takes the 8-element chunks

@@ -19,9 +19,11 @@ float64 variant of the expert loop and a dense brute force for pinning it):
   align    token batching by expert: a stable, block-padded grouping of the
            flat (token, slot) ids by expert ("mini-sglang guide, chapter 7",
            paragraph on ``moe/fused.py``).
-  norm     the residual add + RMSNorm before the MoE ("mini-sglang guide",
-           the decoder layer, RMSNormFused and the torch_ops ``rmsnorm`` /
-           ``fused_add_rmsnorm``), in the pages' rounding order.
+  norm     the residual add + RMSNorm before the MoE ("The op layer: BaseOP
+           and the layers": the ``rmsnorm`` / ``fused_add_rmsnorm`` listings
+           of "Ops: reference implementations and dispatch"; RMSNormFused and
+           ``DecoderLayer.forward`` of "RMSNorm and the residual"), in the
+           pages' rounding order.
   experts  per expert: gate_up projection, SiLU(gate) * up, down projection
            ("模型与权重加载", GatedMLP: gate_up_proj -> silu_and_mul ->
            down_proj, gate rows before up rows; streaming loader, step 4:
@@ -69,8 +71,10 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------ add + RMSNorm ---
 #
-# The step before the MoE in a decoder layer ("mini-sglang guide", decoder
-# layer and RMSNormFused; torch_ops ``rmsnorm`` / ``fused_add_rmsnorm``):
+# The step before the MoE in a decoder layer ("The op layer: BaseOP and the
+# layers", sections "Ops: reference implementations and dispatch" for the
+# ``rmsnorm`` / ``fused_add_rmsnorm`` listings and "RMSNorm and the residual"
+# for RMSNormFused and ``DecoderLayer.forward``):
 # residual <- x + residual (in the bf16 dtype of the tensors); then
 # y = r * rsqrt(mean(r^2) + eps) in float32, rounded to bf16, times the
 # weight, rounded to bf16. The pages leave the order of the float32 sum of
