@@ -225,8 +225,8 @@ def align(ids: np.ndarray, E: int, block_m: int):
 # --------------------------------------------------------------- experts ---
 
 def silu_and_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
-    """silu(g) * u with silu(g) = g / (1 + exp(-g)) ("The op layer" page, the
-    activation; "模型与权重加载", GatedMLP: silu x up)."""
+    """silu(g) * u with silu(g) = g / (1 + exp(-g)) ("模型与权重加载",
+    section 模型结构, GatedMLP: hidden_act "silu", gate_up_proj -> silu x up)."""
     with np.errstate(over="ignore"):
         return g / (1 + np.exp(-g)) * u
 
