@@ -15,20 +15,22 @@
 // so the gate_up epilogue finds g and u of one (row, token) in the same thread.
 //
 // Token rows (B): the contiguous act rows of the down mode come by 2-D TMA
-// boxes. In gate_up mode they are gathered from hidden through
-// sorted_token_ids / k: with few rows per expert (decode-sized batches) by TMA
-// tile::gather4, four rows per instruction; with many rows per expert by four
-// warps of 16-byte cp.async (the TMA engine would spend one gather per four
-// rows of every stage), straight into the swizzled layout. hidden stays in L2,
-// and no permuted copy of the activations is ever written.
+// boxes, and so do gate_up's rows when the layer has copied them into
+// segment order first (many rows per expert). Otherwise gate_up gathers them
+// from hidden through sorted_token_ids / k: with few rows per expert
+// (decode-sized batches) by TMA tile::gather4, four rows per instruction;
+// with many rows per expert (the standalone grouped GEMM) by four warps of
+// 16-byte cp.async straight into the swizzled layout (the TMA engine would
+// spend one gather per four rows of every stage).
 //
 // Warp roles (448 threads, one CTA per SM, persistent over a static tile
 // stride): warp 0 = weight (A) TMA producer, warps 10-13 = token (B) producer
 // (warp 10 alone for TMA), warp 1 = TMEM allocator + MMA issuer, warps 2-9 =
 // epilogue: warps w and w+4 read the same 32-lane quarter of tensor memory
 // and take alternate 32-column chunks of the tile.
-// Two accumulator buffers (256x128 tiles) let the epilogue of one tile
-// overlap the main loop of the next.
+// Two accumulator buffers (256 x BN tiles) let the epilogue of one tile
+// overlap the main loop of the next. BN = 128 with a 4-stage ring, or 64 with
+// a 5-stage ring when there are few rows per expert.
 //
 // Epilogues: gate_up writes act = bf16(silu(g) * u) ("模型与权重加载",
 // GatedMLP: silu_and_mul of the merged gate_up projection, gate first);
