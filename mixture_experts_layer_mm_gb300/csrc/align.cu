@@ -13,9 +13,13 @@
 // pass), then works from there.
 // Small batches (T <= 1024 and T*k <= 8192): one block does histogram, scan
 // and scatter in a single launch (for T <= 64 with per-expert 64-bit token
-// masks instead of ballots: align_tiny, which the router also runs). Otherwise: two launches over blocks of 256
-// tokens (per-block counts; then each block derives its own slot bases from
-// all blocks' counts and scatters); no block ever waits on another.
+// masks instead of ballots: align_tiny, which the router also runs).
+// Otherwise: two launches over blocks of 256 tokens (per-block counts; then
+// each block derives its own slot bases from all blocks' counts and
+// scatters). When the tensor-core router has already counted each of its
+// token tiles, the place step runs alone, from those counts, and in the MoE
+// layer it also copies the token rows into segment order
+// (align_place_rows_kernel). No block ever waits on another.
 #include <algorithm>
 
 #include "align_block.cuh"

@@ -1,7 +1,8 @@
 // The C ABI of include/mm.h: argument checks, the per-device state
 // (SM count, status word, internal workspace) and the launch sequence of the
-// MoE layer. Every computing step runs in the kernels of route.cu, align.cu
-// and gemm.cu; this file only validates, lays out memory and launches.
+// MoE layer. Every computing step runs in the kernels of route.cu,
+// route_tc.cu, align.cu, gemm.cu and norm.cu; this file only validates, lays
+// out memory and launches.
 #include <algorithm>
 #include <mutex>
 

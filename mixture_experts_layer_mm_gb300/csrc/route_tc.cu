@@ -20,8 +20,11 @@
 // wait is a bounded mbarrier wait (no named barriers), so a timeout unwinds
 // all roles.
 //
-// The launch also zeroes the fp32 output accumulator of the layer: every CTA
-// of the grid (one per SM, including those without a tile) clears one slice.
+// The epilogue also counts each tile's experts (tile_counts), from which the
+// grouping places the tokens in one launch. The launch can zero a buffer on
+// the side: every CTA of the grid (one per SM, including those without a
+// tile) clears one slice (the layer passes none: its accumulator is zeroed by
+// the gate_up kernel).
 #include <math.h>
 
 #include "mm_device.cuh"
