@@ -99,7 +99,8 @@ def test_route_and_align_write_only_their_outputs(T, E, k):
 def test_dense_mlp_and_norm_write_only_their_outputs():
     T, H, I = 64, 128, 256
     rng = np.random.default_rng(3)
-    x = Guarded((T, H), torch.bfloat16, torch.randn(T, H, generator=None).to(torch.bfloat16))
+    x = Guarded((T, H), torch.bfloat16,
+                torch.from_numpy(rng.standard_normal((T, H), dtype=np.float32)).to(torch.bfloat16))
     wgu = Guarded((2 * I, H), torch.bfloat16,
                   (0.05 * torch.from_numpy(rng.standard_normal((2 * I, H), dtype=np.float32)))
                   .to(torch.bfloat16))
