@@ -50,7 +50,15 @@ def test_align_capacity(lib):
 def test_workspace_size(lib):
     n = mm.mm_moe_workspace_size(4096, 2048, 128, 768, 8)
     cap = 4096 * 8 + 128 * 15
-    assert n >= cap * 768 * 2 + 4096 * 2048 * 4   # act + fp32 accumulator
+    act, acc = cap * 768 * 2, 4096 * 2048 * 4
+    xs = cap * 2048 * 2                           # token rows in segment order (T*k > 64*E)
+    ids_w, sorted_ = 2 * 4096 * 8 * 4, cap * 4
+    tile_counts = (4096 // 32 + 1) * 128 * 4      # the tensor-core router's per-tile counts
+    assert n >= act + acc + xs + ids_w + sorted_ + tile_counts
+    # decode-sized: rows are gathered inside the GEMM, so no copy of the rows
+    cap_d = 64 * 8 + 128 * 15
+    n_d = mm.mm_moe_workspace_size(64, 2048, 128, 768, 8)
+    assert cap_d * 768 * 2 + 64 * 2048 * 4 <= n_d < cap_d * 2048 * 2
     assert mm.mm_moe_workspace_size(4, 100, 8, 64, 2) == -1   # H % 64
     assert mm.mm_moe_workspace_size(4, 128, 8, 96, 2) == -1   # I % 64
     assert mm.mm_moe_workspace_size(4, 128, 300, 64, 2) == -1  # E > 256
