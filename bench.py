@@ -184,6 +184,24 @@ def algorithmic_work(shape, ids: np.ndarray):
             "layer": {"bytes": layer_bytes, "flops": 2 * T * E * H + 2 * M * 3 * H * I}}
 
 
+def kernel_launches(shape, add_norm: bool = False) -> int:
+    """Kernels one layer call launches for this shape (the launch sequence of
+    the library's forward): route (which also groups when T <= 64), the
+    grouping (one block up to 1024 tokens; count + place beyond; place alone
+    from the tensor-core router's tile counts above 2048 tokens with E <= 128),
+    the row copy into segment order when T*k > 64*E (inside the place launch
+    when it runs from tile counts and E % 4 == 0), gate_up, down, finalize;
+    plus the add + RMSNorm kernel in front when add_norm."""
+    T, E, k = shape.T, shape.E, shape.top_k
+    fused_align = T <= 64 and T * k <= 8192
+    single_align = T <= 1024 and T * k <= 8192
+    router_counts = T > 2048 and E <= 128
+    rows_gathered = T * k > 64 * E
+    separate_copy = rows_gathered and not (router_counts and E % 4 == 0)
+    grouping = 0 if fused_align else 1 if (single_align or router_counts) else 2
+    return 4 + grouping + (1 if separate_copy else 0) + (1 if add_norm else 0)
+
+
 def load_traffic(workload: str, kernel: str):
     if not os.path.exists(TRAFFIC_FILE):
         return None
@@ -577,14 +595,7 @@ def main():
     layer_ms = sum(stage_ms.values())
     roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                      "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
-    fused_align = shape.T <= 64 and shape.T * k <= 8192
-    single_align = shape.T <= 1024 and shape.T * k <= 8192
-    rows_gathered = shape.T * k > 64 * shape.E  # token rows copied into segment order
-    router_counts = shape.T > 2048 and shape.E <= 128  # the grouping is then one launch
-    # with the router's counts and E % 4 == 0 the grouping also copies the rows
-    separate_copy = rows_gathered and not (router_counts and shape.E % 4 == 0)
-    launches_per_step = (4 + (0 if fused_align else 1 if (single_align or router_counts) else 2)
-                         + (1 if separate_copy else 0) + (1 if args.add_norm else 0))
+    launches_per_step = kernel_launches(shape, args.add_norm)
     n_io = 2 if args.add_norm else 1  # x and residual in, out and residual back
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,

@@ -6,6 +6,7 @@ worked out by hand for the Qwen3-30B-A3B-shaped layer (H=2048, E=128, k=8,
 I=768): 6.29 MB of gate/up weights and 3.15 MB of down weights per selected
 expert, 76.0 MFLOP per token for the whole layer.
 """
+import dataclasses
 import os
 import sys
 
@@ -59,3 +60,18 @@ def test_prefill_intensity_is_below_the_measured_ridge():
     intensity = w["gate_up"]["flops"] / w["gate_up"]["bytes"]
     assert intensity == pytest.approx(236.3, rel=1e-3)
     assert intensity < 1904.1e12 / 6783.5e9
+
+
+def test_kernel_launches_follow_the_launch_sequence():
+    # decode (T=64): route with the grouping fused, gate_up, down, finalize;
+    # prefill (T=4096): tensor-core route, grouping + row copy, gate_up, down,
+    # finalize (the kernels profiles/layer_launches_*.md list per pass)
+    assert bench.kernel_launches(S.DECODE) == 4
+    assert bench.kernel_launches(S.PREFILL) == 5
+    assert bench.kernel_launches(S.LARGE) == 5
+    assert bench.kernel_launches(S.DECODE, add_norm=True) == 5
+    # one-block grouping; count + place + a separate row copy; E % 4 != 0
+    assert bench.kernel_launches(S.SWEEP.with_T(512)) == 5
+    assert bench.kernel_launches(S.SWEEP.with_T(2048)) == 7
+    odd_e = dataclasses.replace(S.PREFILL, E=30, top_k=4)
+    assert bench.kernel_launches(odd_e) == 6
