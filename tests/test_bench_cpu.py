@@ -65,7 +65,7 @@ def test_prefill_intensity_is_below_the_measured_ridge():
 def test_kernel_launches_follow_the_launch_sequence():
     # decode (T=64): route with the grouping fused, gate_up, down, finalize;
     # prefill (T=4096): tensor-core route, grouping + row copy, gate_up, down,
-    # finalize (the kernels profiles/layer_launches_*.md list per pass)
+    # finalize (the kernels an ncu launch list shows per pass)
     assert bench.kernel_launches(S.DECODE) == 4
     assert bench.kernel_launches(S.PREFILL) == 5
     assert bench.kernel_launches(S.LARGE) == 5
