@@ -11,6 +11,12 @@ E=128, k=8, I=768): every step streams the selected experts' weights (about
 whose step reads less than twice the L2 size (--sweep-T 1) are timed step by
 step, with an L2-sized write between steps outside the timed events.
 
+The line's value, roofline and e2e are the decode layer's (fraction of the
+HBM copy peak). The same run also times the prefill layer of the same model
+(T=4096) and reports it in the line's prefill_qwen3_30b_a3b object, as
+flops / time against the bf16 tensor peak for the layer, gate_up and down.
+One NVML sampler covers every timed region of the run.
+
 --impl reference times the CPU oracle on the host cores instead (a baseline,
 not a target). Under torchrun every rank runs its own replica (the layer
 shards by tokens with no exchange), and rank 0 prints the line.
@@ -170,18 +176,30 @@ class ClockSampler:
 
 def algorithmic_work(shape, ids: np.ndarray):
     """Algorithmic bytes / flops of the layer and of its two GEMM kernels for
-    one step, from the realised routing (padding, re-reads and the fp32
-    accumulator round trip excluded)."""
+    one step, from the realised routing. Only what the layer has to move
+    counts: each selected expert's weights once, the token rows read once and
+    the output written once. Padding, re-reads, gathers, the act round trip
+    between the GEMMs and the fp32 accumulator traffic are excluded."""
     T, H, E, k, I = shape.T, shape.H, shape.E, shape.top_k, shape.I
     D = int(np.unique(ids).size)          # distinct experts selected in the batch
     M = T * k                             # real (token, expert) rows
-    gu_bytes = D * 2 * I * H * 2 + T * H * 2 + M * I * 2
-    dn_bytes = D * H * I * 2 + M * I * 2 + T * H * 4
+    gu_bytes = D * 2 * I * H * 2 + T * H * 2     # gate/up rows of the selected experts + x
+    dn_bytes = D * H * I * 2 + T * H * 2         # down rows of the selected experts + out
     layer_bytes = D * 3 * H * I * 2 + E * H * 2 + 2 * T * H * 2
     return {"D": D,
             "gate_up": {"bytes": gu_bytes, "flops": 2 * M * H * 2 * I},
             "down": {"bytes": dn_bytes, "flops": 2 * M * I * H},
             "layer": {"bytes": layer_bytes, "flops": 2 * T * E * H + 2 * M * 3 * H * I}}
+
+
+def tensor_regime(shape) -> bool:
+    """Whether the roofline fraction is taken against the bf16 tensor peak
+    (flops / time) rather than the HBM peak (bytes / time): batches with more
+    than 64 rows per expert on average (T*k > 64*E), where the GEMMs read
+    their token rows in segment order and reuse every weight tile across
+    many tokens (prefill, the large config, the sweep from T = 2048). Below
+    that the layer streams the selected experts' weights (decode)."""
+    return shape.T * shape.top_k > 64 * shape.E
 
 
 def kernel_launches(shape, add_norm: bool = False) -> int:
@@ -383,6 +401,185 @@ def run_dense(args, shape, ws, rank, dev, mm):
         print(json.dumps(line), flush=True)
 
 
+def roofline(shape, work, stage_ms, ms, pk, pk_kind):
+    """The roofline object of the dominant kernel (the gate_up grouped GEMM:
+    the largest share of both bytes and flops), and of the whole layer.
+    Decode-shaped batches are measured as algorithmic bytes / time against
+    the HBM copy peak, prefill-shaped ones (tensor_regime) as flops / time
+    against the bf16 burst peak; both fractions are in the object."""
+    dom = "gate_up"
+    dom_ms = stage_ms[dom]
+    bw = work[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
+    tf = work[dom]["flops"] / (dom_ms * 1e-3) / 1e12
+    if tensor_regime(shape):
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
+                "peak_kind": f"{pk_kind} bf16_tflops (burst)"}
+    else:
+        roof = {"bound": "hbm", "achieved": bw, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": bw / pk["hbm_gbs"], "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)"}
+    roof["frac_hbm"] = bw / pk["hbm_gbs"]
+    roof["frac_tensor"] = tf / pk["bf16_tflops"]
+    roof["intensity_flop_per_byte"] = work[dom]["flops"] / work[dom]["bytes"]
+    roof["kernel"] = f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
+    roof["traffic"] = load_traffic(shape.name, dom)
+    dn_ms = stage_ms["down"]
+    roof["down"] = {"frac_hbm": work["down"]["bytes"] / (dn_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                    "frac_tensor": work["down"]["flops"] / (dn_ms * 1e-3) / 1e12 /
+                    pk["bf16_tflops"], "us_per_launch": dn_ms * 1e3}
+    roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                     "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 /
+                     pk["bf16_tflops"]}
+    return roof
+
+
+class LayerRun:
+    """One workload's device inputs and the three timed regions of bench.py:
+    A the layer as a user calls it (device-resident inputs), B the same
+    steps with stage events around each kernel, C end to end from pinned
+    host memory through the C ABI."""
+
+    def __init__(self, mm, shape, dev, weights, bias, rank, add_norm=False, eps=1e-6):
+        self.mm, self.shape, self.dev = mm, shape, dev
+        self.router_w, self.w_gu, self.w_dn = weights
+        self.bias = bias
+        self.add_norm, self.eps = add_norm, eps
+        self.stream = torch.cuda.current_stream(dev)
+        self.hidden = _to_dev(synthetic.make_hidden(replica_batch(shape, rank)), dev)
+        self.out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
+        if add_norm:  # x, the residual stream and the norm weight of the step before
+            nrm = synthetic.make_norm_inputs(rank, shape.T, shape.H)
+            self.x, self.res = _to_dev(nrm["x"], dev), _to_dev(nrm["residual"], dev)
+            self.norm_w = _to_dev(nrm["norm_w"], dev)
+
+    def fwd(self, hidden=None):
+        mm, sh = self.mm, self.shape
+        if self.add_norm:
+            mm.mm_moe_forward_add_norm(self.x if hidden is None else hidden, self.norm_w,
+                                       self.eps, self.router_w, self.w_gu, self.w_dn, sh.top_k,
+                                       sh.renorm, residual=self.res, out=self.out)
+        else:
+            mm.mm_moe_forward(self.hidden if hidden is None else hidden, self.router_w,
+                              self.w_gu, self.w_dn, sh.top_k, sh.renorm, out=self.out,
+                              router_bias=self.bias)
+
+    def warmup(self, n):
+        for _ in range(n):
+            self.fwd()
+        torch.cuda.synchronize()
+
+    def auto_steps(self, seconds=0.6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(5):
+            self.fwd()
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return int(min(5000, max(20, seconds * 1e3 / max(e0.elapsed_time(e1) / 5, 1e-3))))
+
+    def work(self):
+        sh = self.shape
+        ids, _ = self.mm.mm_route(self.hidden, self.router_w, sh.top_k, sh.renorm,
+                                  router_bias=self.bias)
+        return algorithmic_work(sh, ids.cpu().numpy())
+
+    def measure(self, steps, ws, flush_bytes, l2_bytes, e2e=True):
+        """Runs regions A, B (and C); returns ms per step, stage ms, e2e s per step."""
+        mm, stream, dev = self.mm, self.stream, self.dev
+        # A step whose bytes would stay in L2 is timed alone, after a write of
+        # twice the L2 size (outside its events) evicts the previous step's data.
+        flush = flush_bytes < 2 * l2_bytes
+        scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
+        self.flushed = flush
+        # ---- region A
+        barrier(ws)
+        torch.cuda.synchronize()
+        if flush:
+            step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(steps)]
+            for a, b in step_ev:
+                scratch.zero_()
+                a.record(stream)
+                self.fwd()
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in step_ev) / steps
+        else:
+            t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for _ in range(steps):
+                self.fwd()
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            ms = t_start.elapsed_time(t_end) / steps
+        barrier(ws)
+        ms = max_over_ranks(ms, ws, dev)
+        # ---- region B: stage events (the layer itself, without the norm step)
+        sh = self.shape
+        nb = min(steps, 200)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mm.PROFILE_STAGES) + 1)]
+               for _ in range(nb)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        for i in range(nb):
+            if flush:
+                scratch.zero_()  # before the call's first event
+            mm.mm_moe_forward_profiled(self.hidden, self.router_w, self.w_gu, self.w_dn, sh.top_k,
+                                       sh.renorm, evs[i], out=self.out, router_bias=self.bias)
+        torch.cuda.synchronize()
+        barrier(ws)
+        stage_ms = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
+                                          for i in range(nb))
+                    for j, name in enumerate(mm.PROFILE_STAGES)}
+        e2e_s = None
+        if e2e:
+            e2e_s = self._measure_e2e(steps, ws, flush, scratch)
+        st = mm.mm_poll_device_status()
+        if st != mm.MM_OK:
+            raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
+        return ms, stage_ms, e2e_s
+
+    def _measure_e2e(self, steps, ws, flush, scratch):
+        # ---- region C: pinned host -> device, the call, device -> host
+        stream, sh = self.stream, self.shape
+        src = self.x if self.add_norm else self.hidden
+        h_host = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, pin_memory=True)
+        h_host.copy_(src.cpu())
+        o_host = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, pin_memory=True)
+        h_dev = torch.empty_like(src)
+        if self.add_norm:  # the step's inputs are x and the residual; outputs out and residual
+            r_host = torch.empty_like(h_host, pin_memory=True)
+            r_host.copy_(self.res.cpu())
+            r_back = torch.empty_like(h_host, pin_memory=True)
+        self.io_bytes = sh.T * sh.H * 2 * (2 if self.add_norm else 1)
+        barrier(ws)
+        torch.cuda.synchronize()
+        total = 0.0
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            if flush:  # the flush is kept out of the step's wall time
+                scratch.zero_()
+                stream.synchronize()
+                t0 = time.perf_counter()
+            h_dev.copy_(h_host, non_blocking=True)
+            if self.add_norm:
+                self.res.copy_(r_host, non_blocking=True)
+            self.fwd(h_dev)
+            if self.add_norm:
+                r_back.copy_(self.res, non_blocking=True)
+            o_host.copy_(self.out, non_blocking=True)
+            stream.synchronize()
+            if flush:
+                total += time.perf_counter() - t0
+        if not flush:
+            total = time.perf_counter() - t0
+        return max_over_ranks(total / steps, ws, self.dev)
+
+
+def _to_dev(bits, dev):
+    return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,6 +592,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="with the decode workload, skip the prefill measurement that the line "
+                         "carries as its prefill_qwen3_30b_a3b object")
     ap.add_argument("--add-norm", action="store_true",
                     help="time mm_moe_forward_add_norm: the residual add + RMSNorm step "
                          "before the layer, then the layer, in one call")
@@ -433,178 +633,52 @@ def main():
         raise SystemExit("--add-norm takes no router bias (the Zipf sweep has one)")
     # Each replica gets its own batch (hidden seed = rank); the layer weights are shared.
     w = synthetic.make_weights(shape)
-    hid_np = synthetic.make_hidden(replica_batch(shape, rank))
-    bias_np = synthetic.make_router_bias(shape)
-
-    def to_dev(bits):
-        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
-
-    router_w, w_gu, w_dn = to_dev(w["router_w"]), to_dev(w["w_gate_up"]), to_dev(w["w_down"])
+    weights = (_to_dev(w["router_w"], dev), _to_dev(w["w_gate_up"], dev),
+               _to_dev(w["w_down"], dev))
     del w
-    hidden = to_dev(hid_np)
+    bias_np = synthetic.make_router_bias(shape)
     bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
-    out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device=dev)
-    k, renorm = shape.top_k, shape.renorm
-    stream = torch.cuda.current_stream(dev)
-
-    def fwd():
-        mm.mm_moe_forward(hidden, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
-
-    eps = 1e-6
-    if args.add_norm:  # x, the residual stream and the norm weight of the step before
-        nrm = synthetic.make_norm_inputs(rank, shape.T, shape.H)
-        x_d, res_d, nw_d = to_dev(nrm["x"]), to_dev(nrm["residual"]), to_dev(nrm["norm_w"])
-
-        def fwd():  # noqa: F811 - the timed call in this mode
-            mm.mm_moe_forward_add_norm(x_d, nw_d, eps, router_w, w_gu, w_dn, k, renorm,
-                                       residual=res_d, out=out)
-
-
-    for _ in range(args.warmup):
-        fwd()
-    torch.cuda.synchronize()
+    run = LayerRun(mm, shape, dev, weights, bias, rank, add_norm=args.add_norm)
+    run.warmup(args.warmup)
     if args.steps is None:  # size the timed region to about 0.6 s so clocks are sampled
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(5):
-            fwd()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        args.steps = int(min(5000, max(20, 600.0 / max(e0.elapsed_time(e1) / 5, 1e-3))))
-        args.steps = int(max_over_ranks(float(args.steps), ws, dev))
+        args.steps = int(max_over_ranks(float(run.auto_steps()), ws, dev))
     st = mm.mm_poll_device_status()
     if st != mm.MM_OK:
         raise RuntimeError(f"device status after warm-up: {mm.status_string(st)}")
-    ids, _ = mm.mm_route(hidden, router_w, k, renorm, router_bias=bias)
-    work = algorithmic_work(shape, ids.cpu().numpy())
-
-    # ---- timed region A: the layer as a user calls it (device-resident inputs).
-    # A step whose bytes would stay in L2 is timed alone, after a write of
-    # twice the L2 size (outside its events) evicts the previous step's data.
+    work = run.work()
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = work["layer"]["bytes"] < 2 * l2_bytes
-    scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        if flush:
-            step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                       for _ in range(args.steps)]
-            for a, b in step_ev:
-                scratch.zero_()
-                a.record(stream)
-                fwd()
-                b.record(stream)
-        else:
-            t_start.record(stream)
-            for _ in range(args.steps):
-                fwd()
-            t_end.record(stream)
-        torch.cuda.synchronize()
-    barrier(ws)
-    if flush:
-        ms = sum(a.elapsed_time(b) for a, b in step_ev) / args.steps
-    else:
-        ms = t_start.elapsed_time(t_end) / args.steps
-    ms = max_over_ranks(ms, ws, dev)
-    clocks = clk.summary()
-
-    # ---- timed region B: same steps, stage events recorded around each kernel
-    nb = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(mm.PROFILE_STAGES) + 1)]
-           for _ in range(nb)]
-    barrier(ws)
-    torch.cuda.synchronize()
-    for i in range(nb):
-        if flush:
-            scratch.zero_()  # before the call's first event
-        mm.mm_moe_forward_profiled(hidden, router_w, w_gu, w_dn, k, renorm, evs[i], out=out,
-                                   router_bias=bias)
-    torch.cuda.synchronize()
-    barrier(ws)
-    stage_ms = {}
-    for j, name in enumerate(mm.PROFILE_STAGES):
-        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1])
-                                         for i in range(nb))
-
-    # ---- timed region C: end to end from pinned host memory through the C ABI
-    h_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
-    h_host.copy_(hidden.cpu())
-    o_host = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, pin_memory=True)
-    h_dev = torch.empty_like(hidden)
-    if args.add_norm:  # the step's inputs are x and the residual; outputs out and residual
-        r_host = torch.empty_like(h_host, pin_memory=True)
-        r_host.copy_(res_d.cpu())
-        r_back = torch.empty_like(h_host, pin_memory=True)
-    barrier(ws)
-    torch.cuda.synchronize()
-    e2e_total = 0.0
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        if flush:  # the flush is kept out of the step's wall time
-            scratch.zero_()
-            stream.synchronize()
-            t0 = time.perf_counter()
-        h_dev.copy_(h_host, non_blocking=True)
-        if args.add_norm:
-            res_d.copy_(r_host, non_blocking=True)
-            mm.mm_moe_forward_add_norm(h_dev, nw_d, eps, router_w, w_gu, w_dn, k, renorm,
-                                       residual=res_d, out=out)
-            r_back.copy_(res_d, non_blocking=True)
-        else:
-            mm.mm_moe_forward(h_dev, router_w, w_gu, w_dn, k, renorm, out=out, router_bias=bias)
-        o_host.copy_(out, non_blocking=True)
-        stream.synchronize()
-        if flush:
-            e2e_total += time.perf_counter() - t0
-    if not flush:
-        e2e_total = time.perf_counter() - t0
-    e2e_s = max_over_ranks(e2e_total / args.steps, ws, dev)
-    st = mm.mm_poll_device_status()
-    if st != mm.MM_OK:
-        raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
+    # The prefill-shaped layer of the same model, measured in the same run
+    # (the metric's tensor-core half), when the workload is the decode layer.
+    pre = None
+    if shape.name == synthetic.DECODE.name and not args.no_prefill:
+        pre_shape = synthetic.PREFILL
+        pre = LayerRun(mm, pre_shape, dev, weights, None, rank, add_norm=args.add_norm)
+        pre.warmup(args.warmup)
+        pre_steps = int(min(200, max(args.steps, 50)))
+        pre_work = pre.work()
 
     pk, pk_kind = peaks()
+    # One NVML sampler spans every timed region of the run (A, B, C of the
+    # workload, then A and B of the prefill layer).
+    with ClockSampler(local) as clk:
+        ms, stage_ms, e2e_s = run.measure(args.steps, ws, work["layer"]["bytes"], l2_bytes)
+        if pre is not None:
+            pre_ms, pre_stage, _ = pre.measure(pre_steps, ws, pre_work["layer"]["bytes"],
+                                               l2_bytes, e2e=False)
+    clocks = clk.summary()
+
     T_all = shape.T * ws
     value = job_tokens_per_s(shape.T, ws, ms)
-    # The dominant kernel: the gate_up grouped GEMM (largest share of bytes and flops).
-    dom = "gate_up"
-    dom_ms = stage_ms[dom]
-    # The bound is the kernel's arithmetic intensity (algorithmic flops per
-    # algorithmic DRAM byte) against the ridge of the measured peaks; both
-    # fractions are reported.
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    intensity = work[dom]["flops"] / work[dom]["bytes"]
-    bw = work[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
-    tf = work[dom]["flops"] / (dom_ms * 1e-3) / 1e12
-    if intensity < ridge:   # bound by streaming the weights
-        roof = {"bound": "hbm", "achieved": bw, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": bw / pk["hbm_gbs"],
-                "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth)"}
-    else:
-        roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
-                "peak_kind": f"{pk_kind} bf16_tflops (burst)"}
-    roof["intensity_flop_per_byte"] = intensity
-    roof["ridge_flop_per_byte"] = ridge
-    roof["frac_hbm"] = bw / pk["hbm_gbs"]
-    roof["frac_tensor"] = tf / pk["bf16_tflops"]
-    roof["kernel"] = f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
-    roof["traffic"] = load_traffic(shape.name, dom)
-    layer_ms = sum(stage_ms.values())
-    roof["layer"] = {"bytes_frac_hbm": work["layer"]["bytes"] / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                     "flops_frac_bf16": work["layer"]["flops"] / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+    roof = roofline(shape, work, stage_ms, ms, pk, pk_kind)
     launches_per_step = kernel_launches(shape, args.add_norm)
-    n_io = 2 if args.add_norm else 1  # x and residual in, out and residual back
-
+    flush = run.flushed
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded normals, bf16; random-init weights of the named shape)",
             "config": {"workload": shape.name + ("+add_rmsnorm" if args.add_norm else ""),
                        "T": shape.T, "H": shape.H, "E": shape.E,
-                       "top_k": k, "I": shape.I, "renorm": renorm,
+                       "top_k": shape.top_k, "I": shape.I, "renorm": shape.renorm,
                        "distinct_experts": work["D"], "parallelism": f"replicas x{ws}",
                        "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write "
                               "outside each step's events): the step's "
@@ -614,12 +688,26 @@ def main():
                               f"weights ({work['layer']['bytes'] / 1e9:.2f} GB)")},
             "roofline": roof,
             "stage_ms": {n: round(v, 5) for n, v in stage_ms.items()},
-            "stage_sum_ms": layer_ms,
+            "stage_sum_ms": sum(stage_ms.values()),
             "e2e": {"value": T_all / e2e_s, "unit": UNIT,
-                    "h2d_bytes_per_step": int(h_host.numel() * 2 * n_io),
-                    "d2h_bytes_per_step": int(o_host.numel() * 2 * n_io)},
+                    "h2d_bytes_per_step": int(run.io_bytes),
+                    "d2h_bytes_per_step": int(run.io_bytes)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
+    if pre is not None:
+        proof = roofline(pre.shape, pre_work, pre_stage, pre_ms, pk, pk_kind)
+        line[pre.shape.name + ("+add_rmsnorm" if args.add_norm else "")] = {
+            "T": pre.shape.T, "steps": pre_steps, "ms_per_step": pre_ms,
+            "value": job_tokens_per_s(pre.shape.T, ws, pre_ms), "unit": UNIT,
+            "bound": "tensor", "peak": pk["bf16_tflops"], "peak_kind": proof["peak_kind"],
+            "frac_tensor_layer": proof["layer"]["flops_frac_bf16"],
+            "frac_tensor_gate_up": proof["frac_tensor"],
+            "frac_tensor_down": proof["down"]["frac_tensor"],
+            "frac_hbm_layer": proof["layer"]["bytes_frac_hbm"],
+            "stage_ms": {n: round(v, 5) for n, v in pre_stage.items()},
+            "layer_tflops": pre_work["layer"]["flops"] / (pre_ms * 1e-3) / 1e12,
+            "gpu_launches": kernel_launches(pre.shape, args.add_norm) * pre_steps,
+            "traffic_gate_up": proof["traffic"]}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, args.cpu_budget)
     if rank == 0:

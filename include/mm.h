@@ -194,6 +194,42 @@ int mm_moe_forward_ex(const uint16_t* hidden, const uint16_t* router_w,
                       uint16_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Where a call of mm_moe_forward_ex with a caller workspace leaves its
+ * routing and its grouping ("mini-sglang guide, chapter 7": the router's
+ * top-k of layers/moe.py, the token batching by expert of moe/fused.py), so
+ * that the caller can read them after the call's kernels have completed.
+ * Host-only: no CUDA call, nothing allocated.
+ *
+ * layout: a host array of MM_WS_LAYOUT_FIELDS int64 that receives
+ *   [MM_WS_TOPK_IDS]          byte offset of topk_ids [T, top_k] int32 (as mm_route)
+ *   [MM_WS_TOPK_W]            byte offset of topk_w [T, top_k] fp32 (as mm_route)
+ *   [MM_WS_SORTED_TOKEN_IDS]  byte offset of sorted_token_ids [capacity] int32
+ *   [MM_WS_EXPERT_OFFSETS]    byte offset of expert_offsets [E+1] int32
+ *   [MM_WS_EXPERT_COUNTS]     byte offset of expert_counts [E] int32
+ *   [MM_WS_CAPACITY]          capacity = mm_align_capacity(T, top_k, E, block_m)
+ *   [MM_WS_BLOCK_M]           the block_m the forward pads expert segments to
+ *   [MM_WS_TOTAL]             mm_moe_workspace_size(T, H, E, I, top_k)
+ * Offsets are from the start of the workspace and 256-byte aligned. The
+ * grouping is exactly mm_align(topk_ids, T, top_k, E, block_m) (bit for
+ * bit), whichever kernels the forward used for this batch size. The contents
+ * stay valid until the workspace is passed to another call.
+ * Returns MM_OK, or the code mm_moe_workspace_size's checks give
+ * (MM_ERR_INVALID_ARG / MM_ERR_UNSUPPORTED; also for layout == NULL).
+ */
+enum {
+  MM_WS_TOPK_IDS = 0,
+  MM_WS_TOPK_W = 1,
+  MM_WS_SORTED_TOKEN_IDS = 2,
+  MM_WS_EXPERT_OFFSETS = 3,
+  MM_WS_EXPERT_COUNTS = 4,
+  MM_WS_CAPACITY = 5,
+  MM_WS_BLOCK_M = 6,
+  MM_WS_TOTAL = 7,
+  MM_WS_LAYOUT_FIELDS = 8
+};
+int mm_moe_workspace_layout(int T, int H, int E, int I, int top_k, int64_t* layout);
+
+/*
  * The dense SwiGLU MLP, through the same grouped-GEMM kernels: out =
  * down_proj(silu(gate_proj(x)) * up_proj(x)) for every token ("模型与权重加载",
  * GatedMLP; Qwen3 dense layers, and the MoE model's mlp_only_layers named in
@@ -222,8 +258,10 @@ int64_t mm_gated_mlp_workspace_size(int T, int H, int I);
  * With residual == NULL (the first layer) x is the residual and is only read.
  * The float32 sum of squares runs in a fixed order (32 lanes each summing
  * the 8-element chunks c = lane, lane + 32, ... in order, then an xor
- * butterfly) and rsqrt is 1/sqrt with both steps rounded, so normed is
- * bit-reproducible.
+ * butterfly) and rsqrt is 1/sqrt with both steps rounded, so normed is the
+ * same on every call. Against the exact mean of the squares, that float32
+ * sum is off by a few ulps, which can move an element of normed by a bf16
+ * rounding step where it sits on a rounding boundary.
  *
  * x, residual, normed [T,H] bf16 row-major; norm_w [H] bf16; eps >= 0.
  * Caller-owned device pointers, 16-byte aligned; x, residual and normed must

@@ -37,6 +37,7 @@ SIGNATURES = {
     "mm_grouped_gemm": (_I, [_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "mm_moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "mm_moe_workspace_size": (_I64, [_I, _I, _I, _I, _I]),
+    "mm_moe_workspace_layout": (_I, [_I, _I, _I, _I, _I, _P]),
     "mm_moe_forward_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mm_moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
                                      _P]),
@@ -112,6 +113,40 @@ def mm_align_capacity(T: int, top_k: int, E: int, block_m: int) -> int:
 
 def mm_moe_workspace_size(T: int, H: int, E: int, I: int, top_k: int) -> int:
     return int(lib().mm_moe_workspace_size(T, H, E, I, top_k))
+
+
+# Fields of mm_moe_workspace_layout, in the order of its MM_WS_* indices.
+WS_LAYOUT_FIELDS = ("topk_ids", "topk_w", "sorted_token_ids", "expert_offsets", "expert_counts",
+                    "capacity", "block_m", "total")
+
+
+def mm_moe_workspace_layout(T: int, H: int, E: int, I: int, top_k: int) -> dict:
+    """Byte offsets of the routing and grouping inside a caller workspace of
+    mm_moe_forward_ex, plus capacity, block_m and the total size."""
+    buf = (ctypes.c_int64 * len(WS_LAYOUT_FIELDS))()
+    _check(lib().mm_moe_workspace_layout(T, H, E, I, top_k, ctypes.cast(buf, ctypes.c_void_p)),
+           "mm_moe_workspace_layout")
+    return dict(zip(WS_LAYOUT_FIELDS, (int(v) for v in buf)))
+
+
+def forward_routing(workspace, T: int, H: int, E: int, I: int, top_k: int) -> dict:
+    """Views into a caller workspace that mm_moe_forward_ex just used: its
+    own topk_ids, topk_w, sorted_token_ids, expert_offsets and expert_counts
+    (valid once the call's kernels have completed)."""
+    lay = mm_moe_workspace_layout(T, H, E, I, top_k)
+    if workspace.dtype != torch.uint8 or workspace.numel() < lay["total"]:
+        raise ValueError("workspace is not a caller workspace of these sizes")
+
+    def view(name, n, dtype):
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return workspace[lay[name]:lay[name] + nbytes].view(dtype)
+
+    return {"topk_ids": view("topk_ids", T * top_k, torch.int32).view(T, top_k),
+            "topk_w": view("topk_w", T * top_k, torch.float32).view(T, top_k),
+            "sorted_token_ids": view("sorted_token_ids", lay["capacity"], torch.int32),
+            "expert_offsets": view("expert_offsets", E + 1, torch.int32),
+            "expert_counts": view("expert_counts", E, torch.int32),
+            "block_m": lay["block_m"]}
 
 
 def mm_route(hidden, router_w, top_k: int, renorm: bool, router_bias=None,

@@ -326,23 +326,16 @@ long long align_scratch_ints(int T, int E, int k) {
 cudaError_t launch_align(const int32_t* topk_ids, int T, int top_k, int E, int block_m,
                          long long capacity, int32_t* sorted, int32_t* offsets, int32_t* counts,
                          int32_t* scratch, unsigned* err, bool after_prev, cudaStream_t st) {
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
-  if (!attr_done[dev]) {
-    cudaError_t e;
+  {
+    static DeviceFlags single_done, count_done, place_done;
     const int single = (int)align_smem_bytes(32, kMaxExperts, 8);  // 32 warps, E=256, 8192 ids
     const int multi = (int)align_smem_bytes(kAlignBlockTokens / 32, kMaxExperts, kMaxTopK);
-    if ((e = cudaFuncSetAttribute(align_single_kernel,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, single)) !=
-        cudaSuccess)
+    cudaError_t e;
+    if ((e = smem_attr_once(single_done, align_single_kernel, single)) != cudaSuccess ||
+        (e = smem_attr_once(count_done, align_count_kernel, multi)) != cudaSuccess ||
+        (e = smem_attr_once(place_done, align_place_kernel, multi + kMaxExperts * 4)) !=
+            cudaSuccess)
       return e;
-    if ((e = cudaFuncSetAttribute(align_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  multi)) != cudaSuccess)
-      return e;
-    if ((e = cudaFuncSetAttribute(align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  multi + kMaxExperts * 4)) != cudaSuccess)
-      return e;
-    attr_done[dev] = true;
   }
   if (align_single_block(T, top_k)) {
     // T <= 64: the bitmask grouping, with 8 warps; else one warp per 32 tokens.
@@ -369,14 +362,11 @@ cudaError_t launch_align_from_counts(const int32_t* topk_ids, int T, int top_k, 
                                      const int32_t* tile_counts, int tile_tokens, int32_t* sorted,
                                      int32_t* offsets, int32_t* counts, bool after_prev,
                                      cudaStream_t st) {
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
-  if (!attr_done[dev]) {
+  {
+    static DeviceFlags attr_done;
     const int multi = (int)align_smem_bytes(kAlignBlockTokens / 32, kMaxExperts, kMaxTopK);
-    const cudaError_t e = cudaFuncSetAttribute(
-        align_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, multi + kMaxExperts * 4);
+    const cudaError_t e = smem_attr_once(attr_done, align_place_kernel, multi + kMaxExperts * 4);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
   }
   const int nblocks = (T + kAlignBlockTokens - 1) / kAlignBlockTokens;
   const int rows = (T + tile_tokens - 1) / tile_tokens;
@@ -392,15 +382,12 @@ cudaError_t launch_align_place_rows(const int32_t* topk_ids, int T, int top_k, i
                                     int32_t* offsets, int32_t* counts, uint16_t* xs,
                                     bool after_prev, cudaStream_t st) {
   if (E % 4 != 0 || tile_tokens > kPlaceRowsThreads || H % 8 != 0) return cudaErrorInvalidValue;
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
   constexpr int W = kPlaceRowsThreads / 32;
-  if (!attr_done[dev]) {
+  {
+    static DeviceFlags attr_done;
     const size_t most = place_rows_smem_bytes(W, kMaxExperts, 128, kMaxTopK);
-    const cudaError_t e = cudaFuncSetAttribute(
-        align_place_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    const cudaError_t e = smem_attr_once(attr_done, align_place_rows_kernel, (int)most);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
   }
   if (tile_tokens > 128) return cudaErrorInvalidValue;
   const int rows = (T + tile_tokens - 1) / tile_tokens;

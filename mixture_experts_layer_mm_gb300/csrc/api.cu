@@ -229,6 +229,24 @@ int64_t mm_moe_workspace_size(int T, int H, int E, int I, int top_k) {
   return (int64_t)forward_layout(T, H, E, I, top_k).total;
 }
 
+int mm_moe_workspace_layout(int T, int H, int E, int I, int top_k, int64_t* layout) {
+  if (layout == nullptr) return MM_ERR_INVALID_ARG;
+  const int rc = check_route_shape(T, H, E, top_k);
+  if (rc != MM_OK) return rc;
+  if (I <= 0) return MM_ERR_INVALID_ARG;
+  if (I % 64 != 0) return MM_ERR_UNSUPPORTED;
+  const ForwardLayout L = forward_layout(T, H, E, I, top_k);
+  layout[MM_WS_TOPK_IDS] = (int64_t)L.ids;
+  layout[MM_WS_TOPK_W] = (int64_t)L.w;
+  layout[MM_WS_SORTED_TOKEN_IDS] = (int64_t)L.sorted;
+  layout[MM_WS_EXPERT_OFFSETS] = (int64_t)L.offsets;
+  layout[MM_WS_EXPERT_COUNTS] = (int64_t)L.counts;
+  layout[MM_WS_CAPACITY] = (int64_t)L.capacity;
+  layout[MM_WS_BLOCK_M] = kForwardBlockM;
+  layout[MM_WS_TOTAL] = (int64_t)L.total;
+  return MM_OK;
+}
+
 }  // extern "C"
 
 namespace {

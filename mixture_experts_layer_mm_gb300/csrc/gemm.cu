@@ -659,15 +659,11 @@ cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, v
                        int num_sms, unsigned* err, bool after_prev, cudaStream_t st,
                        float* zero_buf, long long zero_count) {
   using Cfg = GemmCfg<MODE, BN, S, NACC, KB>;
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, BN, S, NACC, KB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  static DeviceFlags attr_done;
+  if (cudaError_t e =
+          smem_attr_once(attr_done, grouped_gemm_kernel<MODE, BN, S, NACC, KB>, Cfg::kSmemBytes);
+      e != cudaSuccess)
+    return e;
   GemmArgs a;
   a.sorted = sorted;
   a.offsets = offsets;

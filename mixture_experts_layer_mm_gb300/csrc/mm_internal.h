@@ -2,6 +2,8 @@
 // is include/mm.h and is implemented in api.cu).
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -47,6 +49,24 @@ inline int current_device() {
   int d = 0;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) d = 0;
   return d;
+}
+
+// Per-device first-use flags of kernel attributes. Atomic, so that host
+// threads calling into the library at the same time (with distinct
+// workspaces) read and set them without a data race; two threads that both
+// see the flag unset both set the same attribute value, which CUDA allows.
+using DeviceFlags = std::atomic<bool>[kMaxDevices];
+
+// Raises kern's dynamic shared-memory limit to `bytes` on the current device,
+// once per device.
+template <typename Kern>
+inline cudaError_t smem_attr_once(DeviceFlags& done, Kern kern, int bytes) {
+  const int dev = current_device();
+  if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_release);
+  return e;
 }
 
 // Device address of the current device's status word (see

@@ -11,7 +11,8 @@
 // multiply-add), then an xor butterfly over the lanes (16, 8, 4, 2, 1).
 // rsqrt(v) = 1 / sqrt(v) with both steps rounded. With that order fixed every
 // operation is a correctly rounded float32 step, so the normalised rows are
-// bit-reproducible.
+// the same on every call (the pages leave the summation order open; another
+// order can move an element by one bf16 rounding step).
 #include "mm_device.cuh"
 #include "mm_internal.h"
 

@@ -244,14 +244,9 @@ cudaError_t launch_ep(const uint16_t* hidden, const uint16_t* router_w, const fl
   const size_t gemm_bytes = (size_t)kRtBufs * (kRtTok + EP) * kRtLd * sizeof(uint16_t);
   const size_t recv_bytes = (size_t)kRtTok * EP * sizeof(float);
   const size_t smem = gemm_bytes > recv_bytes ? gemm_bytes : recv_bytes;
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel<EP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  static DeviceFlags attr_done;
+  if (cudaError_t e = smem_attr_once(attr_done, route_kernel<EP>, (int)smem); e != cudaSuccess)
+    return e;
   // Cluster size: the largest of 8, 4, 2 that splits H into 64-wide chunks
   // and keeps the whole grid resident at once (CTAs per SM bounded by shared
   // memory). Small batches get the widest split, which shortens each CTA's

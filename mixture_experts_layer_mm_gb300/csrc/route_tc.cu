@@ -414,14 +414,10 @@ cudaError_t launch_tok(const uint16_t* hidden, const uint16_t* router_w, const f
                        float* zero_buf, long long zero_count, int32_t* tile_counts, int num_sms,
                        unsigned* err, bool after_prev, cudaStream_t st) {
   using Cfg = RcCfg<TOK>;
-  static bool attr_done[kMaxDevices] = {};
-  const int dev = current_device();
-  if (!attr_done[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        route_tc_kernel<TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  static DeviceFlags attr_done;
+  if (cudaError_t e = smem_attr_once(attr_done, route_tc_kernel<TOK>, Cfg::kSmemBytes);
+      e != cudaSuccess)
+    return e;
   CUtensorMap tmR, tmH;
   if (!make_tensor_map_2d(&tmR, router_w, (uint64_t)E, (uint64_t)H, 128, kRcK) ||
       !make_tensor_map_2d(&tmH, hidden, (uint64_t)T, (uint64_t)H, TOK, kRcK))

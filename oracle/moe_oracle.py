@@ -29,12 +29,13 @@ float64 variant of the expert loop and a dense brute force for pinning it):
            down_proj, gate rows before up rows; streaming loader, step 4:
            experts stacked into [E, ...]), then the routing-weighted sum.
 
-Readings taken where the pages are silent (each is listed with its reason in
-the design notes): fp32 logits; softmax over all E before top-k; larger logit
+Readings taken where the pages are silent: fp32 logits (rounding them to
+bf16 would make top-k ties common); softmax over all E before top-k; larger logit
 wins and equal logits go to the lower expert id; slot order within a token is
 ascending expert id; norm_topk_prob divides the selected probabilities by their
 sum; grouping within an expert is by increasing flat id f = t*k + j; padding
-sentinel = T*k; rows [0, I) of w_gate_up[e] are gate, [I, 2I) are up.
+sentinel = T*k; rows [0, I) of w_gate_up[e] are gate, [I, 2I) are up; the
+mean of squares in RMSNorm is the exact mean rounded once to float32.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
 closed forms, invariants, brute force over all k-subsets, a dense masked
@@ -77,36 +78,27 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 # for RMSNormFused and ``DecoderLayer.forward``):
 # residual <- x + residual (in the bf16 dtype of the tensors); then
 # y = r * rsqrt(mean(r^2) + eps) in float32, rounded to bf16, times the
-# weight, rounded to bf16. The pages leave the order of the float32 sum of
-# squares open; the reading taken (design notes) fixes it as: lane l of 32
-# sums, in order, its 8-element chunks c = l, l + 32, l + 64, ... (elements
-# 8c .. 8c+7 in order, each square rounded before the add), then the 32 lane
-# sums are combined by an xor butterfly (offsets 16, 8, 4, 2, 1). rsqrt(v)
-# is read as 1 / sqrt(v), each step rounded to float32.
+# weight, rounded to bf16. The pages fix the mean of the squares but not the
+# order in which a float32 implementation sums them; the oracle takes the
+# plain definition: the sum in float64 (the squares of bf16 values are exact
+# there, and the sum of a few thousand of them is exact to ~1e-13 relative),
+# divided by H and rounded once to float32. An implementation that sums in
+# float32 in any order lands within a few float32 ulps of that mean, so its
+# bf16 outputs may differ from the oracle's by a rounding step where a value
+# sits on a bf16 rounding boundary. rsqrt(v) is read as 1 / sqrt(v), each
+# step rounded to float32.
 
-def sum_of_squares(xf: np.ndarray) -> np.ndarray:
-    """Float32 sum over the last axis of xf**2, in the order stated above."""
-    xf = np.asarray(xf, dtype=np.float32)
-    H = xf.shape[-1]
-    Hp = -(-H // 256) * 256
-    sq = np.zeros(xf.shape[:-1] + (Hp,), dtype=np.float32)
-    sq[..., :H] = xf * xf  # float32 products; zero padding adds exactly 0
-    sq = sq.reshape(xf.shape[:-1] + (Hp // 256, 32, 8))  # [.., round i, lane, element]
-    lanes = np.zeros(xf.shape[:-1] + (32,), dtype=np.float32)
-    for i in range(Hp // 256):
-        for e in range(8):
-            lanes = lanes + sq[..., i, :, e]
-    for o in (16, 8, 4, 2, 1):
-        lanes = lanes + lanes[..., np.arange(32) ^ o]
-    return lanes[..., 0]
+def mean_of_squares(xf: np.ndarray) -> np.ndarray:
+    """mean(xf**2) over the last axis: float64 sum / H, rounded to float32."""
+    x64 = np.asarray(xf, dtype=np.float32).astype(np.float64)
+    return (np.sum(x64 * x64, axis=-1) / x64.shape[-1]).astype(np.float32)
 
 
 def rmsnorm(x_bits: np.ndarray, weight_bits: np.ndarray, eps: float) -> np.ndarray:
     """bf16 rows x [.., H], bf16 weight [H] -> bf16 bit patterns of
     weight * bf16(x * rsqrt(mean(x^2) + eps))."""
     xf = widen_bf16(x_bits)
-    H = xf.shape[-1]
-    mean = sum_of_squares(xf) / np.float32(H)
+    mean = mean_of_squares(xf)
     inv = np.float32(1.0) / np.sqrt(mean + np.float32(eps), dtype=np.float32)
     y = round_bf16(xf * inv[..., None])
     return round_bf16(widen_bf16(weight_bits)[None, :] * widen_bf16(y))

@@ -66,20 +66,25 @@ def check_round_bf16():
 
 # ------------------------------------------------------ add + RMSNorm ---
 
-def check_sum_of_squares():
+def check_mean_of_squares():
     rng = np.random.default_rng(12)
-    # Small integers: every partial sum is an exact float32 integer, so any
-    # summation order gives the exact sum.
-    for H in (64, 192, 2048, 4096):
+    # Small integers and H a power of two: the exact mean is a short binary
+    # fraction, representable in float32, so the result must equal it.
+    for H in (64, 2048, 4096):
         x = rng.integers(-3, 4, size=(5, H)).astype(np.float32)
-        assert np.array_equal(O.sum_of_squares(x), (x.astype(np.int64) ** 2).sum(1)
-                              .astype(np.float32))
-    # Random rows: within the float32 error bound of a sum of n terms
-    # (n - 1 additions, each off by at most half an ulp of the partial sum).
-    x = rng.standard_normal((7, 4096)).astype(np.float32)
-    got = O.sum_of_squares(x).astype(np.float64)
-    exact = np.array([math.fsum((r.astype(np.float64) ** 2).tolist()) for r in x])
-    assert (np.abs(got - exact) <= 4096 * 2.0 ** -24 * exact).all()
+        exact = (x.astype(np.int64) ** 2).sum(1) / H
+        assert np.array_equal(O.mean_of_squares(x), exact.astype(np.float32))
+    # Random rows (H not a power of two too): the exactly rounded float32 of
+    # math.fsum's correctly rounded sum / H, to within one float32 rounding.
+    for H in (192, 4096):
+        x = rng.standard_normal((7, H)).astype(np.float32) * 30
+        got = O.mean_of_squares(x).astype(np.float64)
+        exact = np.array([math.fsum((r.astype(np.float64) ** 2).tolist()) / H for r in x])
+        assert (np.abs(got - exact) <= 2.0 ** -24 * exact).all()
+    # One element carries the whole sum: mean = v^2 / H exactly (H = 2^k).
+    x = np.zeros((1, 1024), np.float32)
+    x[0, 777] = 3.0
+    assert O.mean_of_squares(x)[0] == np.float32(9.0 / 1024)
 
 
 def _textbook_rmsnorm(r_bits, w_bits, eps):

@@ -64,6 +64,27 @@ def test_workspace_size(lib):
     assert mm.mm_moe_workspace_size(4, 128, 300, 64, 2) == -1  # E > 256
 
 
+def test_workspace_layout(lib):
+    for (T, H, E, I, k) in [(4096, 2048, 128, 768, 8), (64, 2048, 128, 768, 8), (16, 128, 8, 64, 2),
+                            (2600, 64, 160, 64, 4), (0, 64, 8, 64, 2)]:
+        lay = mm.mm_moe_workspace_layout(T, H, E, I, k)
+        assert lay["total"] == mm.mm_moe_workspace_size(T, H, E, I, k)
+        assert lay["block_m"] == mm.FORWARD_BLOCK_M
+        assert lay["capacity"] == mm.mm_align_capacity(T, k, E, lay["block_m"])
+        regions = sorted([(lay["topk_ids"], T * k * 4), (lay["topk_w"], T * k * 4),
+                          (lay["sorted_token_ids"], lay["capacity"] * 4),
+                          (lay["expert_offsets"], (E + 1) * 4), (lay["expert_counts"], E * 4)])
+        for (o, n), (o2, _) in zip(regions, regions[1:] + [(lay["total"], 0)]):
+            assert o % 256 == 0 and o + n <= o2, (T, H, E, I, k, regions)
+    with pytest.raises(mm.MMError) as ei:
+        mm.mm_moe_workspace_layout(4, 128, 8, 96, 2)
+    assert ei.value.code == mm.MM_ERR_UNSUPPORTED
+    with pytest.raises(mm.MMError) as ei:
+        mm.mm_moe_workspace_layout(-1, 128, 8, 64, 2)
+    assert ei.value.code == mm.MM_ERR_INVALID_ARG
+    assert lib.mm_moe_workspace_layout(4, 128, 8, 64, 2, None) == mm.MM_ERR_INVALID_ARG
+
+
 def test_host_checks_before_any_cuda_call(lib):
     L = mm.lib()
     # null pointers

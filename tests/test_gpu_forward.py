@@ -5,6 +5,19 @@ is too slow for the whole batch (T*I*H large), it is evaluated on a sample of
 tokens (routing is per token, so a token's output depends only on its own
 row); the routing and grouping are still compared on the whole batch.
 
+The forward runs with a caller workspace, and the routing and grouping
+compared here are the ones the forward itself computed and used (read from
+that workspace at the offsets mm_moe_workspace_layout gives), whichever
+kernels it chose for the batch size: the grouping fused into the router
+(T <= 64), the one-block grouping (T <= 1024), count + place (up to 2048
+tokens, or more than 128 experts), and the grouping from the tensor-core
+router's per-tile counts (above 2048 tokens), with the token-row copy in the
+same launch (E % 4 == 0) or after it. Expert ids must equal the oracle's on
+every token whose k-th and (k+1)-th logits differ by more than 1e-4; the
+grouping must equal the oracle's grouping of the forward's ids bit for bit;
+the routing weights must match the oracle's weights of those ids within
+W_RTOL.
+
 The output is compared with the oracle's expert step taken on the GPU's own
 routing (the conditional oracle) and, where no token is a near tie, with the
 unconditional oracle, within max|err| <= 2e-2 max|ref| and mean relative
@@ -19,7 +32,7 @@ from mixture_experts_layer_mm_gb300.synthetic import (DECODE, LARGE, PREFILL, SW
                                                       TINY, MoEShape, make_inputs,
                                                       random_small_inputs)
 from oracle import moe_oracle as O
-from gpu_util import TIE_GAP, assert_out_close, dev_bf16, f32_dev
+from gpu_util import TIE_GAP, W_ATOL, W_RTOL, assert_out_close, dev_bf16, f32_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -44,25 +57,44 @@ def _inputs(shape: MoEShape):
 
 
 def _run(d, dev_w, k, renorm):
+    """One forward with a caller workspace; returns out and the routing and
+    grouping the forward left in that workspace."""
     hidden = dev_bf16(d["hidden"])
+    T, H = hidden.shape
+    E, I = dev_w["router_w"].shape[0], dev_w["w_down"].shape[2]
     bias = None if d["router_bias"] is None else f32_dev(d["router_bias"])
+    ws = torch.empty(mm.mm_moe_workspace_size(T, H, E, I, k), dtype=torch.uint8, device="cuda")
     out = mm.mm_moe_forward(hidden, dev_w["router_w"], dev_w["w_gate_up"], dev_w["w_down"], k,
-                            renorm, router_bias=bias)
-    ids, _ = mm.mm_route(hidden, dev_w["router_w"], k, renorm, router_bias=bias)
+                            renorm, router_bias=bias, workspace=ws)
     torch.cuda.synchronize()
     assert mm.mm_poll_device_status() == mm.MM_OK
-    return out.float().cpu().numpy(), ids.cpu().numpy()
+    r = mm.forward_routing(ws, T, H, E, I, k)
+    got = {n: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for n, v in r.items()}
+    return out.float().cpu().numpy(), got
 
 
-def _check(d, k, renorm, out_g, ids_g, sample=None):
+def _check(d, k, renorm, out_g, r_g, sample=None):
     T = d["hidden"].shape[0]
+    E = d["router_w"].shape[0]
+    ids_g, w_g = r_g["topk_ids"], r_g["topk_w"]
     ids_r, w_r, logits = O.route(d["hidden"], d["router_w"], k, renorm, d["router_bias"])
     tie = O.near_tie_tokens(logits, k, TIE_GAP)
+    # ids: equal to the oracle's wherever the choice is unique, and valid everywhere
     assert np.array_equal(ids_g[~tie], ids_r[~tie])
+    assert ids_g.min() >= 0 and ids_g.max() < E
+    assert (np.diff(ids_g, axis=1) > 0).all(), "ids of a token must be distinct and ascending"
+    # weights: the oracle's formula applied to the forward's ids
+    probs_all = O.softmax_over_experts(logits)
+    w_ids_g = O.routing_weights(probs_all, ids_g, renorm)
+    np.testing.assert_allclose(w_g, w_ids_g, rtol=W_RTOL, atol=W_ATOL)
+    # grouping: bit for bit the oracle's grouping of the forward's ids (the
+    # oracle's own ids when no token is a near tie)
+    s_r, off_r, cnt_r = O.align(ids_r if not tie.any() else ids_g, E, r_g["block_m"])
+    assert np.array_equal(r_g["expert_counts"], cnt_r), "expert_counts"
+    assert np.array_equal(r_g["expert_offsets"], off_r), "expert_offsets"
+    assert np.array_equal(r_g["sorted_token_ids"], s_r), "sorted_token_ids"
     tok = np.arange(T) if sample is None else sample
-    probs = O.softmax_over_experts(logits[tok])
-    w_c = O.routing_weights(probs, ids_g[tok], renorm)
-    ref = O.experts_loop(d["hidden"][tok], d["w_gate_up"], d["w_down"], ids_g[tok], w_c)
+    ref = O.experts_loop(d["hidden"][tok], d["w_gate_up"], d["w_down"], ids_g[tok], w_ids_g[tok])
     assert_out_close(out_g[tok], ref, "out (conditional oracle)")
     if not tie[tok].any():
         ref_u = O.experts_loop(d["hidden"][tok], d["w_gate_up"], d["w_down"], ids_r[tok], w_r[tok])
@@ -79,23 +111,23 @@ def _sample(T, n, seed=0):
 @pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
 def test_forward_workloads(shape):
     d, w = _inputs(shape)
-    out, ids = _run(d, w, shape.top_k, shape.renorm)
-    _check(d, shape.top_k, shape.renorm, out, ids, _sample(shape.T, 4096))
+    out, r = _run(d, w, shape.top_k, shape.renorm)
+    _check(d, shape.top_k, shape.renorm, out, r, _sample(shape.T, 4096))
 
 
 def test_forward_large_sampled():
     d, w = _inputs(LARGE)
-    out, ids = _run(d, w, LARGE.top_k, LARGE.renorm)
-    _check(d, LARGE.top_k, LARGE.renorm, out, ids, _sample(LARGE.T, 192))
+    out, r = _run(d, w, LARGE.top_k, LARGE.renorm)
+    _check(d, LARGE.top_k, LARGE.renorm, out, r, _sample(LARGE.T, 192))
 
 
 @pytest.mark.parametrize("T", SWEEP_T)
 def test_forward_zipf_sweep(T):
     shape = SWEEP.with_T(T)
     d, w = _inputs(shape)
-    out, ids = _run(d, w, shape.top_k, shape.renorm)
-    _check(d, shape.top_k, shape.renorm, out, ids, _sample(T, 1024))
-    load = np.bincount(ids.reshape(-1), minlength=shape.E)
+    out, r = _run(d, w, shape.top_k, shape.renorm)
+    _check(d, shape.top_k, shape.renorm, out, r, _sample(T, 1024))
+    load = np.bincount(r["topk_ids"].reshape(-1), minlength=shape.E)
     if T >= 512:  # the bias skews the load: the busiest expert gets far more than the mean
         assert load.max() >= 3 * load.mean()
 
@@ -105,6 +137,7 @@ def test_forward_zipf_sweep(T):
     (37, 128, 6, 1, 128, True),   # k = 1
     (50, 192, 8, 8, 64, False),   # every expert on every token
     (129, 256, 40, 5, 192, True), # E not a power of two, partial m-tiles
+    (1000, 128, 64, 8, 64, True), # the one-block grouping at its largest token count
     (300, 64, 256, 32, 64, False),
     (2000, 128, 16, 4, 320, True),
     # above 2048 tokens the tensor-core router also writes per-tile expert
@@ -120,8 +153,8 @@ def test_forward_zipf_sweep(T):
 def test_forward_shapes(T, H, E, k, I, renorm):
     d = random_small_inputs(T + 3 * E, T, H, E, I, w_std=0.08, bias=(E % 2 == 0))
     dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
-    out, ids = _run(d, dw, k, renorm)
-    _check(d, k, renorm, out, ids)
+    out, r = _run(d, dw, k, renorm)
+    _check(d, k, renorm, out, r)
 
 
 def test_forward_closed_forms():

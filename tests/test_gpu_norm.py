@@ -1,11 +1,16 @@
 """GPU parity of the residual add + RMSNorm step (mm_add_rmsnorm) and of the
 MoE layer behind it (mm_moe_forward_add_norm) against the CPU oracle.
 
-The step is a chain of correctly rounded float32 operations in an order both
-sides fix (design notes), so the new residual and the normalised rows must be
+The new residual is one correctly rounded bf16 add on both sides, so it must
+be bit-exact. For the normalised rows the oracle takes the exact mean of the
+squares, rounded once to float32, and the kernel its own float32 sum: they
+must agree within NORM_MAX_STEPS bf16 steps, and differ at all only on a
+small fraction of the elements (gpu_util states the bound and its reason).
+Rows whose sum of squares is exact in float32 (the hand-worked case) must be
 bit-exact. The layer's output is then compared as in test_gpu_forward: with
-the oracle's expert step on the GPU's own routing, and with the plain oracle
-on tokens that are not near ties.
+the oracle's expert step on the GPU's own normalised rows and routing, and
+with the plain oracle on tokens whose rows match bit for bit and are not
+near ties.
 """
 import json
 import os
@@ -18,7 +23,7 @@ import mixture_experts_layer_mm_gb300 as mm
 from mixture_experts_layer_mm_gb300.synthetic import (DECODE, PREFILL, TINY, make_inputs,
                                                       make_norm_inputs)
 from oracle import moe_oracle as O
-from gpu_util import TIE_GAP, assert_out_close, dev_bf16
+from gpu_util import TIE_GAP, assert_norm_rows_close, assert_out_close, dev_bf16
 
 pytestmark = pytest.mark.gpu
 EPS = 1e-6
@@ -37,14 +42,14 @@ def _bits(t: torch.Tensor) -> np.ndarray:
 @pytest.mark.parametrize("T,H", [(1, 64), (37, 128), (5, 192), (64, 2048), (300, 4096),
                                  (4096, 2048)])
 @pytest.mark.parametrize("with_residual", [True, False])
-def test_add_rmsnorm_bit_exact(T, H, with_residual):
+def test_add_rmsnorm(T, H, with_residual):
     d = make_norm_inputs(T + H, T, H)
     res = dev_bf16(d["residual"]) if with_residual else None
     normed = mm.mm_add_rmsnorm(dev_bf16(d["x"]), dev_bf16(d["norm_w"]), EPS, residual=res)
     torch.cuda.synchronize()
     want_n, want_r = O.fused_add_rmsnorm(d["x"], d["residual"] if with_residual else None,
                                          d["norm_w"], EPS)
-    assert np.array_equal(_bits(normed), want_n)
+    assert_norm_rows_close(_bits(normed), want_n)
     if with_residual:
         assert np.array_equal(_bits(res), want_r)
 
@@ -73,7 +78,7 @@ def test_add_rmsnorm_large_values():
     torch.cuda.synchronize()
     want_n, want_r = O.fused_add_rmsnorm(d["x"], d["residual"], d["norm_w"], EPS)
     assert np.array_equal(_bits(res), want_r)
-    assert np.array_equal(_bits(normed), want_n)
+    assert_norm_rows_close(_bits(normed), want_n)
 
 
 @pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
@@ -97,19 +102,26 @@ def test_moe_forward_add_norm(shape):
 
     normed, r = O.fused_add_rmsnorm(n["x"], n["residual"], n["norm_w"], EPS)
     assert np.array_equal(_bits(res), r)
-    assert np.array_equal(_bits(normed_g), normed)
-    ids_r, w_r, logits = O.route(normed, w["router_w"], k, shape.renorm)
-    tie = O.near_tie_tokens(logits, k, TIE_GAP)
-    assert np.array_equal(ids_g[~tie], ids_r[~tie])
+    normed_gb = _bits(normed_g)
+    assert_norm_rows_close(normed_gb, normed)
+    # The layer's routing: the oracle's on the GPU's own normalised rows.
+    ids_c, _, logits_c = O.route(normed_gb, w["router_w"], k, shape.renorm)
+    tie = O.near_tie_tokens(logits_c, k, TIE_GAP)
+    assert np.array_equal(ids_g[~tie], ids_c[~tie])
     tok = np.arange(T)
     if T > 1024:
         rng = np.random.default_rng(0)
         tok = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 1024, replace=False)]))
-    probs = O.softmax_over_experts(logits[tok])
+    probs = O.softmax_over_experts(logits_c[tok])
     w_c = O.routing_weights(probs, ids_g[tok], shape.renorm)
-    ref = O.experts_loop(normed[tok], w["w_gate_up"], w["w_down"], ids_g[tok], w_c)
+    ref = O.experts_loop(normed_gb[tok], w["w_gate_up"], w["w_down"], ids_g[tok], w_c)
     assert_out_close(out[tok], ref, "out (conditional oracle)")
-    keep = tok[~tie[tok]]
+    # The plain oracle end to end, on tokens whose rows the two sides
+    # normalised identically and whose routing is not a near tie.
+    ids_r, w_r, logits = O.route(normed, w["router_w"], k, shape.renorm)
+    same = (normed_gb == normed).all(axis=1)
+    keep = tok[same[tok] & ~O.near_tie_tokens(logits, k, TIE_GAP)[tok]]
+    assert keep.size >= 0.75 * tok.size
     ref_u = O.experts_loop(normed[keep], w["w_gate_up"], w["w_down"], ids_r[keep], w_r[keep])
     assert_out_close(out[keep], ref_u, "out (oracle, non-tie tokens)")
 
@@ -120,13 +132,15 @@ def test_moe_forward_add_norm_first_layer():
     w = make_inputs(shape)
     n = make_norm_inputs(3, shape.T, shape.H)
     dw = {name: dev_bf16(w[name]) for name in ("router_w", "w_gate_up", "w_down")}
-    x = dev_bf16(n["x"])
-    out = mm.mm_moe_forward_add_norm(x, dev_bf16(n["norm_w"]), EPS, dw["router_w"],
-                                     dw["w_gate_up"], dw["w_down"], shape.top_k, shape.renorm)
+    x, nw = dev_bf16(n["x"]), dev_bf16(n["norm_w"])
+    out = mm.mm_moe_forward_add_norm(x, nw, EPS, dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                                     shape.top_k, shape.renorm)
+    normed_g = _bits(mm.mm_add_rmsnorm(x, nw, EPS))
     torch.cuda.synchronize()
     assert np.array_equal(_bits(x), n["x"])
     normed, _ = O.fused_add_rmsnorm(n["x"], None, n["norm_w"], EPS)
-    ids_r, w_r, logits = O.route(normed, w["router_w"], shape.top_k, shape.renorm)
+    assert_norm_rows_close(normed_g, normed)
+    ids_r, w_r, logits = O.route(normed_g, w["router_w"], shape.top_k, shape.renorm)
     keep = ~O.near_tie_tokens(logits, shape.top_k, TIE_GAP)
-    ref = O.experts_loop(normed[keep], w["w_gate_up"], w["w_down"], ids_r[keep], w_r[keep])
+    ref = O.experts_loop(normed_g[keep], w["w_gate_up"], w["w_down"], ids_r[keep], w_r[keep])
     assert_out_close(out.float().cpu().numpy()[keep], ref, "out (first layer)")

@@ -11,7 +11,7 @@ from oracle import moe_oracle as O
 _orig = {n: getattr(O, n) for n in ("silu_and_mul", "select_topk", "routing_weights",
                                     "softmax_over_experts", "router_logits", "align",
                                     "experts_loop", "widen_bf16", "round_bf16",
-                                    "sum_of_squares", "rmsnorm", "fused_add_rmsnorm")}
+                                    "mean_of_squares", "rmsnorm", "fused_add_rmsnorm")}
 
 
 def _swap_gate_up(g, u):
@@ -125,8 +125,8 @@ def _round_ties_up(x):
     return ((b + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
 
 
-def _sumsq_drop_last(xf):
-    return _orig["sum_of_squares"](np.asarray(xf)[..., :-1])
+def _meansq_drop_last(xf):
+    return _orig["mean_of_squares"](np.asarray(xf)[..., :-1])
 
 
 def _rms_no_eps(x, w, eps):
@@ -135,14 +135,15 @@ def _rms_no_eps(x, w, eps):
 
 def _rms_sum_not_mean(x, w, eps):
     xf = O.widen_bf16(x)
-    inv = np.float32(1.0) / np.sqrt(O.sum_of_squares(xf) + np.float32(eps), dtype=np.float32)
+    total = O.mean_of_squares(xf) * np.float32(xf.shape[-1])
+    inv = np.float32(1.0) / np.sqrt(total + np.float32(eps), dtype=np.float32)
     y = O.round_bf16(xf * inv[..., None])
     return O.round_bf16(O.widen_bf16(w)[None, :] * O.widen_bf16(y))
 
 
 def _rms_single_round(x, w, eps):
     xf = O.widen_bf16(x)
-    mean = O.sum_of_squares(xf) / np.float32(xf.shape[-1])
+    mean = O.mean_of_squares(xf)
     inv = np.float32(1.0) / np.sqrt(mean + np.float32(eps), dtype=np.float32)
     return O.round_bf16(O.widen_bf16(w)[None, :] * (xf * inv[..., None]))
 
@@ -159,7 +160,7 @@ def _add_keeps_old_residual(x, r, w, eps):
 MUTANTS = {
     "round_truncate": ("round_bf16", _round_truncate),
     "round_ties_up": ("round_bf16", _round_ties_up),
-    "sumsq_drop_last": ("sum_of_squares", _sumsq_drop_last),
+    "meansq_drop_last": ("mean_of_squares", _meansq_drop_last),
     "rms_no_eps": ("rmsnorm", _rms_no_eps),
     "rms_sum_not_mean": ("rmsnorm", _rms_sum_not_mean),
     "rms_single_round": ("rmsnorm", _rms_single_round),
