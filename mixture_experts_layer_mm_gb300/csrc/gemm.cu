@@ -1,5 +1,9 @@
 // Grouped expert GEMMs of the MoE layer on the sm_103a tensor cores
 // (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+// This file's kernel serves batches with few token rows per expert (decode:
+// rows gathered from hidden) and the standalone GEMM's gathered rows; token
+// rows already in segment order with many rows per expert (prefill) go to
+// the SM-pair kernel of gemm_pair.cu.
 //
 // Orientation: the expert WEIGHTS are the MMA's M side (128 rows per MMA)
 // and the expert's TOKENS are the N side. N may be any multiple of 16 up to
@@ -24,10 +28,16 @@
 // spend one gather per four rows of every stage).
 //
 // Warp roles (448 threads, one CTA per SM, persistent over a static tile
-// stride): warp 0 = weight (A) TMA producer, warps 10-13 = token (B) producer
-// (warp 10 alone for TMA), warp 1 = TMEM allocator + MMA issuer, warps 2-9 =
-// epilogue: warps w and w+4 read the same 32-lane quarter of tensor memory
-// and take alternate 32-column chunks of the tile.
+// stride): warp 1 = TMEM allocator + MMA issuer, warps 2-9 = epilogue
+// (warps w and w+4 read the same 32-lane quarter of tensor memory and take
+// alternate 32-column chunks of the tile), warps 10-13 and 0 = producers,
+// one per ring slot: slot s is filled by warp 10 + s (slot 4 by warp 0),
+// which issues the slot's weight boxes and its token rows against the
+// slot's barrier. A warp's TMA loads that signal a different barrier than
+// its previous ones wait for those to land, so a single producer warp would
+// keep only one stage in flight; one warp per slot keeps them all in flight.
+// (Token rows copied by cp.async, the standalone GEMM's path for many rows
+// per expert, use warp 0 for the weights and warps 10-13 for the rows.)
 // Two accumulator buffers (256 x BN tiles) let the epilogue of one tile
 // overlap the main loop of the next. BN = 128 with a 4-stage ring, or 64 with
 // a 5-stage ring when there are few rows per expert.
@@ -48,8 +58,8 @@ namespace mm {
 namespace {
 
 constexpr int kGM = 128;  // weight rows per MMA
-// 14 warps: 0 = weight producer, 1 = MMA issuer, 2-9 = epilogue (two warps per
-// tensor-memory lane quarter), 10-13 = token producers.
+// 14 warps: 1 = MMA issuer, 2-9 = epilogue (two warps per tensor-memory lane
+// quarter), 10-13 and 0 = producers (one per ring slot).
 constexpr int kEpiWarp0 = 2, kEpiWarps = 8, kEpiThreads = kEpiWarps * 32;
 constexpr int kBWarp0 = kEpiWarp0 + kEpiWarps;  // 10
 constexpr int kGemmThreads = (kBWarp0 + 4) * 32;  // 448
@@ -109,6 +119,7 @@ struct GemmCfg {
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
   static_assert(BN % 64 == 0 && BN <= 256, "BN: whole 32-column chunks for both epilogue sides");
+  static_assert(S <= 5, "one producer warp per ring slot: warps 10-13, then warp 0");
   static_assert(kSmemBytes <= 227 * 1024 - 4096, "shared memory");
 };
 
@@ -253,7 +264,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // the weight producer + the token side (one TMA producer or 128 loaders)
-      mbar_init(smem_u32(&full[s]), 1 + (a.b_mode == kBLsuGather ? 128 : 1));
+      // one producer warp per slot, or the weight producer + 128 cp.async threads
+      mbar_init(smem_u32(&full[s]), a.b_mode == kBLsuGather ? 1 + 128 : 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < NACC; ++b) {
@@ -277,8 +289,80 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = tmem_base_s;
   const int nk = a.K / KB / a.ksplit;  // K steps per tile (its slice of K)
 
-  if (warp == 0) {
-    // --------------------------------------------- weight (A) TMA producer ---
+  // Producers. A warp's TMA loads that signal a different mbarrier than its
+  // previous ones wait for those to land, so one warp issuing every stage
+  // has at most one stage in flight at a time. Here each ring slot has a
+  // warp of its own (slot s: warp 10 + s, slot 4: warp 0), which issues the
+  // slot's weight boxes and its token rows against the slot's one barrier;
+  // the S slots fill concurrently. (Token rows gathered by cp.async, the
+  // standalone GEMM's path for many rows per expert, keep warp 0 for the
+  // weights and warps 10-13 for the rows.)
+  const bool owners = a.b_mode != kBLsuGather;
+  const int slot = warp == 0 ? 4 : warp - kBWarp0;  // the slot a producer warp owns
+  if (owners && (warp == 0 || warp >= kBWarp0)) {
+    if (slot < S) {
+      const uint64_t pol_w = a.w_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+      const uint64_t pol_x = l2_policy_evict_last();
+      const bool gather = MODE == MM_GEMM_GATE_UP && a.b_mode == kBTmaGather;
+      // Gathered token rows: lane i loads rows 4i..4i+3 of the chunk with one
+      // tile::gather4; the rows of the next tile are fetched a tile ahead.
+      int nxt[4] = {0, 0, 0, 0};
+      auto fetch_rows = [&](int tl, int (&rows)[4]) {
+        int e, m, row0, nrows, slice;
+        if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;
+          const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
+          rows[j] = f < a.Tk ? f / a.top_k : 0;  // padding rows read row 0 (never stored)
+        }
+      };
+      if (gather) fetch_rows(blockIdx.x, nxt);
+      uint32_t use = 0;  // fills of this warp's slot so far
+      int q = 0;         // this CTA's K step counter, modulo S
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        if (aborted(&abort_s)) break;
+        int rows[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
+        if (gather) fetch_rows(tile + gridDim.x, nxt);
+        int e, m, row0, nrows, slice;
+        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
+        const int wrow0 = e * a.w_rows + m * a.m_step;
+        const int wrow1 = wrow0 + a.a1_off;
+        const int n_g4 = ((nrows + 15) & ~15) / 4;  // gathered rows the MMA reads, 4 per gather
+        const uint32_t bbytes = gather ? (uint32_t)(n_g4 * 4 * Cfg::kRowBytes) : Cfg::kBBytes;
+        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
+          const bool mine = q == slot;
+          if (++q == S) q = 0;
+          if (!mine) continue;
+          bool w_ok = true;
+          if (lane == 0) w_ok = mbar_wait(smem_u32(&empty[slot]), (use & 1u) ^ 1u);
+          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          if (!w_ok) {
+            if (lane == 0) signal_abort(&abort_s, a.err);
+            ok = false;
+            break;
+          }
+          const uint32_t st = smem_base + slot * Cfg::kStageBytes;
+          const uint32_t fb = smem_u32(&full[slot]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, 2 * Cfg::kABytes + bbytes);
+            tma_load_2d(st, &tmW, fb, kb * KB, wrow0, pol_w);
+            tma_load_2d(st + Cfg::kABytes, &tmW, fb, kb * KB, wrow1, pol_w);
+            if (!gather) tma_load_2d(st + 2 * Cfg::kABytes, &tmX, fb, kb * KB, row0, pol_x);
+          }
+          if (gather) {
+            __syncwarp();
+            if (lane < n_g4)
+              tma_gather4(st + 2 * Cfg::kABytes + lane * 4 * Cfg::kRowBytes, &tmX, fb, kb * KB,
+                          rows[0], rows[1], rows[2], rows[3], pol_x);
+          }
+          ++use;
+        }
+      }
+    }
+  } else if (warp == 0) {
+    // ----------------------- weight (A) producer of the cp.async token path ---
     if (lane == 0) {
       const uint64_t pol_w = a.w_evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
       int s = 0;
@@ -310,139 +394,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp >= kBWarp0) {
-    // -------------------------------------------------- token (B) producer ---
+    // ------------------------------------ token (B) rows by cp.async (4 warps) ---
+    // Warps 10-13 copy the chunk's token rows from hidden with 16-byte
+    // cp.async into the swizzled layout the MMA reads (16-byte chunk c of
+    // row r at r*RB + ((c ^ sw(r)) * 16), RB = row bytes, sw(r) = r % 8 for
+    // the 128-byte swizzle and (r / 2) % 4 for the 64-byte one). Thread
+    // (w, l) moves chunk l % CPR of rows p*RPP + w*(32/CPR) + l/CPR. Each
+    // thread's copies arrive on the stage's barrier by themselves when they
+    // land (cp.async.mbarrier.arrive.noinc, 128 arrivals per stage); the MMA
+    // thread then fences the generic-to-async proxy before reading.
     const uint64_t pol_x = l2_policy_evict_last();
     int s = 0;
     uint32_t ph = 0;
-    if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBLsuGather) {
-      // Warps 10-13 copy the chunk's token rows from hidden with 16-byte
-      // cp.async into the swizzled layout the MMA reads (16-byte chunk c of
-      // row r at r*RB + ((c ^ sw(r)) * 16), RB = row bytes, sw(r) = r % 8 for
-      // the 128-byte swizzle and (r / 2) % 4 for the 64-byte one). Thread
-      // (w, l) moves chunk l % CPR of rows p*RPP + w*(32/CPR) + l/CPR. Each
-      // thread's copies arrive on the stage's barrier by themselves when they
-      // land (cp.async.mbarrier.arrive.noinc, 128 arrivals per stage); the MMA
-      // thread then fences the generic-to-async proxy before reading.
-      constexpr int kCPR = KB / 8;            // 16-byte chunks per row
-      constexpr int kRPP = 128 / kCPR;        // rows per pass of the 128 threads
-      constexpr int kPasses = BN / kRPP;
-      const int w = warp - kBWarp0, c16 = lane % kCPR;
-      const uint16_t* src[kPasses];
-      const uint16_t* nxt[kPasses];
-      auto fetch_rows = [&](int tl, const uint16_t* (&rows)[kPasses]) {
-        int e, m, row0, nrows, slice;
-        if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
+    constexpr int kCPR = KB / 8;            // 16-byte chunks per row
+    constexpr int kRPP = 128 / kCPR;        // rows per pass of the 128 threads
+    constexpr int kPasses = BN / kRPP;
+    const int w = warp - kBWarp0, c16 = lane % kCPR;
+    const uint16_t* src[kPasses];
+    const uint16_t* nxt[kPasses];
+    auto fetch_rows = [&](int tl, const uint16_t* (&rows)[kPasses]) {
+      int e, m, row0, nrows, slice;
+      if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) {
+        const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
+        const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
+        rows[p] = f < a.Tk ? a.hidden + (size_t)(f / a.top_k) * a.K + c16 * 8 : nullptr;
+      }
+    };
+    fetch_rows(blockIdx.x, nxt);
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      if (aborted(&abort_s)) break;
+#pragma unroll
+      for (int p = 0; p < kPasses; ++p) src[p] = nxt[p];
+      fetch_rows(tile + gridDim.x, nxt);
+      const int slice = tile % a.ksplit;
+      for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
+        if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          if (lane == 0) signal_abort(&abort_s, a.err);
+          break;
+        }
+        const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
 #pragma unroll
         for (int p = 0; p < kPasses; ++p) {
           const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
-          const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
-          rows[p] = f < a.Tk ? a.hidden + (size_t)(f / a.top_k) * a.K + c16 * 8 : nullptr;
+          const int sw = KB == 64 ? (r & 7) : ((r >> 1) & 3);
+          const uint32_t dst = st + r * Cfg::kRowBytes + ((c16 ^ sw) << 4);
+          cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * KB : a.hidden,
+                           src[p] != nullptr, pol_x);
         }
-      };
-      fetch_rows(blockIdx.x, nxt);
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        if (aborted(&abort_s)) break;
-#pragma unroll
-        for (int p = 0; p < kPasses; ++p) src[p] = nxt[p];
-        fetch_rows(tile + gridDim.x, nxt);
-        const int slice = tile % a.ksplit;
-        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
-          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            if (lane == 0) signal_abort(&abort_s, a.err);
-            break;
-          }
-          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
-#pragma unroll
-          for (int p = 0; p < kPasses; ++p) {
-            const int r = p * kRPP + w * (32 / kCPR) + lane / kCPR;
-            const int sw = KB == 64 ? (r & 7) : ((r >> 1) & 3);
-            const uint32_t dst = st + r * Cfg::kRowBytes + ((c16 ^ sw) << 4);
-            cp_async16_zfill(dst, src[p] != nullptr ? src[p] + kb * KB : a.hidden,
-                             src[p] != nullptr, pol_x);
-          }
-          cp_async_arrive_noinc(smem_u32(&full[s]));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
+        cp_async_arrive_noinc(smem_u32(&full[s]));
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
         }
-      }
-      cp_async_wait<0>();  // no copy of this thread is in flight when the CTA ends
-    } else if (warp != kBWarp0) {
-      // Warps 11-13 help only on the cp.async path.
-    } else if (MODE == MM_GEMM_GATE_UP && a.b_mode == kBTmaGather) {
-      // Token rows are gathered straight from hidden: lane i loads rows
-      // 4i..4i+3 of the chunk with one tile::gather4 per stage. The rows of the
-      // next tile are fetched one tile ahead so their latency is hidden.
-      int nxt[4];
-      auto fetch_rows = [&](int tl, int (&rows)[4]) {
-        int e, m, row0, nrows, slice;
-        if (tl < total_tiles) decode_tile_k<BN>(tl, a, E, cs_s, off_s, e, m, row0, nrows, slice);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = 4 * lane + j;
-          const int f = (tl < total_tiles && r < nrows) ? __ldg(a.sorted + row0 + r) : a.Tk;
-          rows[j] = f < a.Tk ? f / a.top_k : 0;  // padding rows read row 0 (never stored)
-        }
-      };
-      fetch_rows(blockIdx.x, nxt);
-      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        if (aborted(&abort_s)) break;
-        int rows[4] = {nxt[0], nxt[1], nxt[2], nxt[3]};
-        fetch_rows(tile + gridDim.x, nxt);
-        int e, m, row0, nrows, slice;
-        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
-        const int n_g4 = ((nrows + 15) & ~15) / 4;  // rows the MMA reads, 4 per gather
-        const uint32_t bytes = n_g4 * 4 * Cfg::kRowBytes;
-        bool ok = true;
-        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
-          if (lane == 0) ok = mbar_wait(smem_u32(&empty[s]), ph ^ 1u);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) {
-            if (lane == 0) signal_abort(&abort_s, a.err);
-            break;
-          }
-          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
-          const uint32_t fb = smem_u32(&full[s]);
-          if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
-          __syncwarp();
-          if (lane < n_g4)
-            tma_gather4(st + lane * 4 * Cfg::kRowBytes, &tmX, fb, kb * KB, rows[0], rows[1], rows[2],
-                        rows[3], pol_x);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-      }
-    } else if (lane == 0) {
-      for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-        if (aborted(&abort_s)) break;
-        int e, m, row0, nrows, slice;
-        decode_tile_k<BN>(tile, a, E, cs_s, off_s, e, m, row0, nrows, slice);
-        bool ok = true;
-        for (int kb = slice * nk; kb < (slice + 1) * nk; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u)) {
-            signal_abort(&abort_s, a.err);
-            ok = false;
-            break;
-          }
-          const uint32_t st = smem_base + s * Cfg::kStageBytes + 2 * Cfg::kABytes;
-          const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, Cfg::kBBytes);
-          tma_load_2d(st, &tmX, fb, kb * KB, row0, pol_x);
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
       }
     }
+    cp_async_wait<0>();  // no copy of this thread is in flight when the CTA ends
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer ---
     if (lane == 0) {
@@ -651,6 +662,23 @@ bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tensor_map_sw128(CUtensorMap* m, const void* base, uint32_t rank,
+                           const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || rank < 2 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], estr[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 template <int MODE, int BN, int S, int NACC, int KB>
 cudaError_t launch_cfg(const uint16_t* X, bool x_is_hidden, const uint16_t* W, void* C,
@@ -799,6 +827,12 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
   // With few rows per expert (the decode regime, where gate_up gathers its
   // rows from hidden) the token tile is at most 64 rows, and the 8 KB it
   // frees per stage buys a fifth stage: more weight bytes in flight per SM.
+  // Many rows per expert, read in segment order (the layer's row copy and
+  // act, a dense MLP's hidden): the SM-pair kernel (gemm_pair.cu).
+  if (!gate_up_gathers_rows(T, top_k, E) && (mode == MM_GEMM_DOWN || !x_is_hidden))
+    return launch_grouped_gemm_pair(mode, X, W, C, sorted, offsets, topk_w, T, top_k, E, N, K,
+                                    capacity, x_rows, num_sms, err, after_prev, st, zero_buf,
+                                    zero_count);
   if (gate_up_gathers_rows(T, top_k, E)) {
     if (mode == MM_GEMM_GATE_UP)
       return launch_cfg<MM_GEMM_GATE_UP, 64, 5, 2, 64>(X, x_is_hidden, W, C, sorted, offsets,

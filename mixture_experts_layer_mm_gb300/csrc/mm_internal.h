@@ -146,6 +146,13 @@ cudaError_t launch_identity_grouping(int T, int block_m, long long capacity, int
 bool make_tensor_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows, int kb);
 
+// Tensor map of a bf16 tensor of `rank` (2..5) dimensions, dims[0] the
+// contiguous one, strides[i] the byte stride of dimension i + 1, read in
+// boxes of box[] elements with the 128-byte swizzle (box[0] * 2 == 128).
+// Elements outside the dimensions read as zeros.
+bool make_tensor_map_sw128(CUtensorMap* m, const void* base, uint32_t rank,
+                           const uint64_t* dims, const uint64_t* strides, const uint32_t* box);
+
 // Whether the gate_up GEMM gathers token rows with TMA tile::gather4 (few rows
 // per expert) rather than with cp.async loader warps.
 bool gate_up_gathers_rows(int T, int top_k, int E);
@@ -163,6 +170,16 @@ cudaError_t launch_grouped_gemm(int mode, const uint16_t* X, bool x_is_hidden, c
                                 long long capacity, long long x_rows, int num_sms, unsigned* err,
                                 bool after_prev, cudaStream_t st, float* zero_buf = nullptr,
                                 long long zero_count = 0);
+
+// The same grouped GEMM on SM pairs (tcgen05 cta_group::2): for token rows
+// already in segment order and many rows per expert. X = xs (gate_up) or
+// act (down) [x_rows, K]; otherwise as launch_grouped_gemm (no split K).
+cudaError_t launch_grouped_gemm_pair(int mode, const uint16_t* X, const uint16_t* W, void* C,
+                                     const int32_t* sorted, const int32_t* offsets,
+                                     const float* topk_w, int T, int top_k, int E, int N, int K,
+                                     long long capacity, long long x_rows, int num_sms,
+                                     unsigned* err, bool after_prev, cudaStream_t st,
+                                     float* zero_buf, long long zero_count);
 
 // out[i] = bf16(acc[i]) for i < n (n % 4 == 0).
 // xs[r] = hidden[sorted[r] / top_k] (H bf16 per row) for r < offsets[E];
