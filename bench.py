@@ -208,8 +208,9 @@ def kernel_launches(shape, add_norm: bool = False) -> int:
     grouping (one block up to 1024 tokens; count + place beyond; place alone
     from the tensor-core router's tile counts above 2048 tokens with E <= 128),
     the row copy into segment order when T*k > 64*E (inside the place launch
-    when it runs from tile counts and E % 4 == 0), gate_up, down, finalize;
-    plus the add + RMSNorm kernel in front when add_norm."""
+    when it runs from tile counts and E % 4 == 0), gate_up, down, finalize
+    (which also adds the residual after the layer in the add-norm mode); plus
+    the add + RMSNorm kernel in front when add_norm."""
     T, E, k = shape.T, shape.E, shape.top_k
     fused_align = T <= 64 and T * k <= 8192
     single_align = T <= 1024 and T * k <= 8192
@@ -454,10 +455,11 @@ class LayerRun:
 
     def fwd(self, hidden=None):
         mm, sh = self.mm, self.shape
-        if self.add_norm:
-            mm.mm_moe_forward_add_norm(self.x if hidden is None else hidden, self.norm_w,
-                                       self.eps, self.router_w, self.w_gu, self.w_dn, sh.top_k,
-                                       sh.renorm, residual=self.res, out=self.out)
+        if self.add_norm:  # both residual adds; the residual stream is updated in place
+            mm.mm_moe_forward_add_norm_residual(self.x if hidden is None else hidden, self.norm_w,
+                                                self.eps, self.router_w, self.w_gu, self.w_dn,
+                                                sh.top_k, sh.renorm, residual=self.res,
+                                                out=self.out)
         else:
             mm.mm_moe_forward(self.hidden if hidden is None else hidden, self.router_w,
                               self.w_gu, self.w_dn, sh.top_k, sh.renorm, out=self.out,
@@ -596,8 +598,9 @@ def main():
                     help="with the decode workload, skip the prefill measurement that the line "
                          "carries as its prefill_qwen3_30b_a3b object")
     ap.add_argument("--add-norm", action="store_true",
-                    help="time mm_moe_forward_add_norm: the residual add + RMSNorm step "
-                         "before the layer, then the layer, in one call")
+                    help="time mm_moe_forward_add_norm_residual: the residual add + RMSNorm "
+                         "step before the layer, the layer, and the residual add after it, "
+                         "in one call")
     ap.add_argument("--dense", action="store_true",
                     help="time mm_gated_mlp: a dense SwiGLU MLP of H x k*I on the workload's "
                          "tokens (the same flops per token as the MoE layer's experts)")

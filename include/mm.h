@@ -283,13 +283,36 @@ int mm_moe_forward_add_norm(const uint16_t* x, uint16_t* residual, const uint16_
                             int renorm, uint16_t* out, void* stream);
 
 /*
+ * The MoE half of a decoder layer with both residual adds ("The op layer:
+ * BaseOP and the layers", "RMSNorm and the residual": DecoderLayer.forward
+ * adds the residual before post_attention_layernorm, and the next layer's
+ * fused_add_rmsnorm adds the MLP output to it):
+ *   residual'    = bf16(x + residual), normed = rmsnorm(residual')
+ *                  (as mm_moe_forward_add_norm; residual == NULL: residual' = x)
+ *   out          = mm_moe_forward(normed, ...)
+ *   residual_out = bf16(out + residual')   (out rounded to bf16 first)
+ * The last add runs in the same pass that rounds the layer's fp32 sum into
+ * out (one read of the sum and of residual', one write of out and of
+ * residual_out). residual_out [T,H] bf16 is required; it may be
+ * residual itself (in-place update of the residual stream) but must not
+ * overlap x or out. The next layer then needs only an RMSNorm of
+ * residual_out (mm_add_rmsnorm with residual == NULL).
+ */
+int mm_moe_forward_add_norm_residual(const uint16_t* x, uint16_t* residual,
+                                     const uint16_t* norm_w, float eps, const uint16_t* router_w,
+                                     const uint16_t* w_gate_up, const uint16_t* w_down, int T,
+                                     int H, int E, int I, int top_k, int renorm, uint16_t* out,
+                                     uint16_t* residual_out, void* stream);
+
+/*
  * Stage timing of mm_moe_forward_ex, for profiling. Same arguments, plus
  * `events`: a host array of MM_PROFILE_EVENTS cudaEvent_t handles (created
  * by the caller with timing enabled). events[i] is recorded on `stream`
  * before stage i and events[5] after the last one; the stages are
  * 0 route (which also does the grouping when T <= 64), 1 align (then
- * empty), 2 gate_up GEMM, 3 down GEMM, 4 fp32 -> bf16 rounding. No stage is skipped or changed; nothing is
- * synchronised. (Measurement support: the pages describe no counterpart.)
+ * empty), 2 gate_up GEMM, 3 down GEMM, 4 fp32 -> bf16 rounding. No stage is
+ * skipped or changed; nothing is synchronised. (Measurement support: the
+ * pages describe no counterpart.)
  */
 #define MM_PROFILE_EVENTS 6
 int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,

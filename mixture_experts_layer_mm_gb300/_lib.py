@@ -46,6 +46,8 @@ SIGNATURES = {
     "mm_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _I, _I, _P, _P]),
     "mm_moe_forward_add_norm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I, _I, _I,
                                      _I, _P, _P]),
+    "mm_moe_forward_add_norm_residual": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _I, _I, _I,
+                                              _I, _I, _I, _P, _P, _P]),
     "mm_poll_device_status": (_I, [_P]),
     "mm_selftest_wait_timeout": (_I, [_P]),
     "mm_shutdown": (None, []),
@@ -301,6 +303,30 @@ def mm_moe_forward_add_norm(x, norm_w, eps: float, router_w, w_gate_up, w_down, 
                                          _ptr(out, torch.bfloat16, "out"), _stream(stream)),
            "mm_moe_forward_add_norm")
     return out
+
+
+def mm_moe_forward_add_norm_residual(x, norm_w, eps: float, router_w, w_gate_up, w_down,
+                                     top_k: int, renorm: bool, residual=None, residual_out=None,
+                                     out=None, stream=None):
+    """The MoE half of a decoder layer: residual' = bf16(x + residual) (in
+    place; x when residual is None), out = layer(rmsnorm(residual')), and
+    residual_out = bf16(out + residual') (default: residual itself, updated
+    in place; a new tensor when residual is None). Returns (out, residual_out)."""
+    T, H = x.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    if residual_out is None:
+        residual_out = residual if residual is not None else torch.empty_like(x)
+    _check(lib().mm_moe_forward_add_norm_residual(
+        _ptr(x, torch.bfloat16, "x"), _ptr(residual, torch.bfloat16, "residual"),
+        _ptr(norm_w, torch.bfloat16, "norm_w"), float(eps),
+        _ptr(router_w, torch.bfloat16, "router_w"), _ptr(w_gate_up, torch.bfloat16, "w_gate_up"),
+        _ptr(w_down, torch.bfloat16, "w_down"), T, H, E, I, top_k, int(bool(renorm)),
+        _ptr(out, torch.bfloat16, "out"), _ptr(residual_out, torch.bfloat16, "residual_out"),
+        _stream(stream)), "mm_moe_forward_add_norm_residual")
+    return out, residual_out
 
 
 PROFILE_STAGES = ("route", "align", "gate_up", "down", "finalize")

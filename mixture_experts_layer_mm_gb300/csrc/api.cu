@@ -251,12 +251,14 @@ int mm_moe_workspace_layout(int T, int H, int E, int I, int top_k, int64_t* layo
 
 namespace {
 
-// The add + RMSNorm step before the layer (see mm_moe_forward_add_norm).
+// The add + RMSNorm step before the layer (see mm_moe_forward_add_norm),
+// and optionally the residual add after it (res_out = bf16(out + residual')).
 struct NormIn {
   const uint16_t* x;
   uint16_t* residual;  // NULL: x is the residual
   const uint16_t* weight;
   float eps;
+  uint16_t* res_out;   // NULL: no add after the layer
 };
 
 // The launch sequence of the layer. If `ev` is non-null, events ev[0..5] are
@@ -279,7 +281,8 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
       !aligned16(w_down) || !aligned16(out))
     return MM_ERR_INVALID_ARG;
   if (norm != nullptr && (!norm->weight || !aligned16(norm->weight) ||
-                          (norm->residual && !aligned16(norm->residual)) || !(norm->eps >= 0.f)))
+                          (norm->residual && !aligned16(norm->residual)) || !(norm->eps >= 0.f) ||
+                          (norm->res_out && !aligned16(norm->res_out))))
     return MM_ERR_INVALID_ARG;
   const ForwardLayout L = forward_layout(T, H, E, I, top_k, true, norm != nullptr);
   if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
@@ -364,7 +367,15 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
                           H, I, L.capacity, L.capacity, s->sms, s->status, true, st) != cudaSuccess ||
       !mark(4))
     return MM_ERR_CUDA;
-  if (launch_finalize(acc, out, nacc, s->sms, true, st) != cudaSuccess || !mark(5))
+  // The rounding of the sum, and with a residual output the add that follows
+  // the layer, in one pass.
+  const uint16_t* res_in = nullptr;
+  uint16_t* res_out = nullptr;
+  if (norm != nullptr && norm->res_out != nullptr) {
+    res_in = norm->residual != nullptr ? norm->residual : norm->x;
+    res_out = norm->res_out;
+  }
+  if (launch_finalize(acc, out, nacc, s->sms, true, st, res_in, res_out) != cudaSuccess || !mark(5))
     return MM_ERR_CUDA;
   return MM_OK;
 }
@@ -464,7 +475,18 @@ int mm_moe_forward_add_norm(const uint16_t* x, uint16_t* residual, const uint16_
                             float eps, const uint16_t* router_w, const uint16_t* w_gate_up,
                             const uint16_t* w_down, int T, int H, int E, int I, int top_k,
                             int renorm, uint16_t* out, void* stream) {
-  const NormIn norm = {x, residual, norm_w, eps};
+  const NormIn norm = {x, residual, norm_w, eps, nullptr};
+  return forward_impl(nullptr, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                      out, nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, &norm);
+}
+
+int mm_moe_forward_add_norm_residual(const uint16_t* x, uint16_t* residual,
+                                     const uint16_t* norm_w, float eps, const uint16_t* router_w,
+                                     const uint16_t* w_gate_up, const uint16_t* w_down, int T,
+                                     int H, int E, int I, int top_k, int renorm, uint16_t* out,
+                                     uint16_t* residual_out, void* stream) {
+  if (T > 0 && residual_out == nullptr) return MM_ERR_INVALID_ARG;
+  const NormIn norm = {x, residual, norm_w, eps, residual_out};
   return forward_impl(nullptr, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm,
                       out, nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, &norm);
 }

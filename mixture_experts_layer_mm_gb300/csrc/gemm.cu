@@ -793,16 +793,33 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+}
+// bf16(o + r) for the two bf16 pairs packed in o and r.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t o, uint32_t r) {
+  return bf16x2_bits(__uint_as_float(o << 16) + __uint_as_float(r << 16),
+                     __uint_as_float(o & 0xFFFF0000u) + __uint_as_float(r & 0xFFFF0000u));
+}
+
+// out = bf16(acc), rounded once; with res_out also the residual add that
+// follows the layer, res_out = bf16(out + res_in) (out rounded first, then
+// the sum, as a bf16 tensor add does; res_out may be res_in).
 __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
-                                                       uint2* __restrict__ out, long long n4) {
+                                                       uint2* __restrict__ out, long long n4,
+                                                       const uint2* res_in, uint2* res_out) {
   pdl_wait();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     const float4 v = acc[i];
     uint2 o;
-    o.x = (uint32_t)f32_to_bf16_bits(v.x) | ((uint32_t)f32_to_bf16_bits(v.y) << 16);
-    o.y = (uint32_t)f32_to_bf16_bits(v.z) | ((uint32_t)f32_to_bf16_bits(v.w) << 16);
+    o.x = bf16x2_bits(v.x, v.y);
+    o.y = bf16x2_bits(v.z, v.w);
     out[i] = o;
+    if (res_out != nullptr) {
+      const uint2 r = res_in[i];
+      res_out[i] = make_uint2(add_bf16x2(o.x, r.x), add_bf16x2(o.y, r.y));
+    }
   }
 }
 
@@ -862,14 +879,16 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
 }
 
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
-                            bool after_prev, cudaStream_t st) {
+                            bool after_prev, cudaStream_t st, const uint16_t* res_in,
+                            uint16_t* res_out) {
   const long long n4 = n / 4;
   long long blocks = (n4 + 255) / 256;
   const long long cap_blocks = (long long)num_sms * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
   if (blocks < 1) blocks = 1;
   return launch_k(finalize_kernel, dim3((int)blocks), dim3(256), 0, st, after_prev,
-                  reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(out), n4);
+                  reinterpret_cast<const float4*>(acc), reinterpret_cast<uint2*>(out), n4,
+                  reinterpret_cast<const uint2*>(res_in), reinterpret_cast<uint2*>(res_out));
 }
 
 }  // namespace mm

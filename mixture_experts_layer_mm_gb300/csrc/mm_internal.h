@@ -188,8 +188,10 @@ cudaError_t launch_gather_rows(const uint16_t* hidden, const int32_t* sorted,
                                const int32_t* offsets, int T, int top_k, int E, int H,
                                uint16_t* xs, int num_sms, bool after_prev, cudaStream_t st);
 
+// With res_out (n elements, may be res_in): res_out = bf16(out + res_in).
 cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int num_sms,
-                            bool after_prev, cudaStream_t st);
+                            bool after_prev, cudaStream_t st, const uint16_t* res_in = nullptr,
+                            uint16_t* res_out = nullptr);
 
 // residual' = bf16(x + residual) in place (residual NULL: x is the residual),
 // normed = rmsnorm(residual', weight, eps) [T, H] bf16. H % 8 == 0.

@@ -147,6 +147,19 @@ def test_add_norm_host_checks(lib):
                                      1, None, None) == mm.MM_OK
 
 
+def test_moe_block_residual_host_checks(lib):
+    import ctypes
+    L = mm.lib()
+    f = ctypes.c_float
+    # residual_out is required; misaligned residual_out; T == 0 is a no-op
+    assert L.mm_moe_forward_add_norm_residual(16, None, 16, f(1e-6), 16, 16, 16, 4, 64, 8, 64, 2,
+                                              1, 16, None, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_moe_forward_add_norm_residual(16, None, 16, f(1e-6), 16, 16, 16, 4, 64, 8, 64, 2,
+                                              1, 16, 8, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_moe_forward_add_norm_residual(None, None, None, f(1e-6), None, None, None, 0, 64,
+                                              8, 64, 2, 1, None, None, None) == mm.MM_OK
+
+
 def test_binding_raises_without_library(monkeypatch, tmp_path):
     import mixture_experts_layer_mm_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)

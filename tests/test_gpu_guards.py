@@ -116,3 +116,23 @@ def test_dense_mlp_and_norm_write_only_their_outputs():
     _check_all(("x", x), ("w_gate_up", wgu), ("w_down", wdn), ("out", out), ("norm_w", nw),
                ("residual", res), ("normed", normed))
     assert torch.equal(res.t, x.t)  # residual' = x + 0
+
+
+@pytest.mark.parametrize("T,H,E,k,I", [(64, 256, 32, 8, 128), (3000, 64, 100, 8, 64)])
+def test_moe_block_with_residual_adds_writes_only_its_outputs(T, H, E, k, I):
+    # The add + RMSNorm step, the layer (SM-pair GEMMs for the 3000-token
+    # batch) and the add after it, which the down GEMM performs.
+    d = random_small_inputs(T + 3 * E, T, H, E, I, w_std=0.08)
+    x = Guarded((T, H), torch.bfloat16, _bf16(d["hidden"]))
+    res = Guarded((T, H), torch.bfloat16, 0.5 * _bf16(d["hidden"]).flip(0))
+    nw = Guarded((H,), torch.bfloat16, torch.ones(H, dtype=torch.bfloat16))
+    rw = Guarded((E, H), torch.bfloat16, _bf16(d["router_w"]))
+    wgu = Guarded((E, 2 * I, H), torch.bfloat16, _bf16(d["w_gate_up"]))
+    wdn = Guarded((E, H, I), torch.bfloat16, _bf16(d["w_down"]))
+    out = Guarded((T, H), torch.bfloat16)
+    r2 = Guarded((T, H), torch.bfloat16)
+    mm.mm_moe_forward_add_norm_residual(x.t, nw.t, 1e-6, rw.t, wgu.t, wdn.t, k, True,
+                                        residual=res.t, residual_out=r2.t, out=out.t)
+    _check_all(("x", x), ("residual", res), ("norm_w", nw), ("router_w", rw),
+               ("w_gate_up", wgu), ("w_down", wdn), ("out", out), ("residual_out", r2))
+    assert torch.isfinite(out.t.float()).all() and torch.isfinite(r2.t.float()).all()

@@ -144,3 +144,64 @@ def test_moe_forward_add_norm_first_layer():
     keep = ~O.near_tie_tokens(logits, shape.top_k, TIE_GAP)
     ref = O.experts_loop(normed_g[keep], w["w_gate_up"], w["w_down"], ids_r[keep], w_r[keep])
     assert_out_close(out.float().cpu().numpy()[keep], ref, "out (first layer)")
+
+
+def _bf16_add(a_bits, b_bits):
+    """bf16(a + b) of two bf16 tensors (a correctly rounded float32 add of
+    exact widenings, as a bf16 tensor add does)."""
+    return O.round_bf16(O.widen_bf16(a_bits) + O.widen_bf16(b_bits))
+
+
+@pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
+@pytest.mark.parametrize("in_place", [True, False])
+def test_moe_forward_add_norm_residual(shape, in_place):
+    # DecoderLayer.forward's order: residual' = x + residual, the MoE block on
+    # rmsnorm(residual'), then the next add: residual'' = out + residual'.
+    T, H, k = shape.T, shape.H, shape.top_k
+    w = make_inputs(shape)
+    n = make_norm_inputs(shape.seed + 29, T, H)
+    dw = {name: dev_bf16(w[name]) for name in ("router_w", "w_gate_up", "w_down")}
+    x, nw = dev_bf16(n["x"]), dev_bf16(n["norm_w"])
+    res = dev_bf16(n["residual"])
+    res_out = None if in_place else torch.empty_like(res)
+    out, r2 = mm.mm_moe_forward_add_norm_residual(x, nw, EPS, dw["router_w"], dw["w_gate_up"],
+                                                  dw["w_down"], k, shape.renorm, residual=res,
+                                                  residual_out=res_out)
+    normed_g = mm.mm_add_rmsnorm(x, nw, EPS, residual=dev_bf16(n["residual"]))
+    torch.cuda.synchronize()
+    assert mm.mm_poll_device_status() == mm.MM_OK
+    assert (r2.data_ptr() == res.data_ptr()) == in_place
+    normed, r1 = O.fused_add_rmsnorm(n["x"], n["residual"], n["norm_w"], EPS)
+    out_b = _bits(out)
+    # the add after the layer: bit for bit on the layer's own output
+    assert np.array_equal(_bits(r2), _bf16_add(out_b, r1))
+    if not in_place:
+        assert np.array_equal(_bits(res), r1)  # residual' left in residual
+    # the layer's output against the oracle on the GPU's normalised rows
+    normed_gb = _bits(normed_g)
+    assert_norm_rows_close(normed_gb, normed)
+    ids_c, _, logits_c = O.route(normed_gb, w["router_w"], k, shape.renorm)
+    tok = np.arange(T)
+    if T > 1024:
+        rng = np.random.default_rng(1)
+        tok = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 1024, replace=False)]))
+    keep = tok[~O.near_tie_tokens(logits_c, k, TIE_GAP)[tok]]
+    probs = O.softmax_over_experts(logits_c[keep])
+    w_c = O.routing_weights(probs, ids_c[keep], shape.renorm)
+    ref = O.experts_loop(normed_gb[keep], w["w_gate_up"], w["w_down"], ids_c[keep], w_c)
+    assert_out_close(O.widen_bf16(out_b)[keep], ref, "out (oracle on the GPU's normed rows)")
+
+
+def test_moe_forward_add_norm_residual_first_layer():
+    # No residual yet: residual' = x, and residual_out = bf16(out + x).
+    shape = TINY
+    w = make_inputs(shape)
+    n = make_norm_inputs(31, shape.T, shape.H)
+    dw = {name: dev_bf16(w[name]) for name in ("router_w", "w_gate_up", "w_down")}
+    x = dev_bf16(n["x"])
+    out, r2 = mm.mm_moe_forward_add_norm_residual(x, dev_bf16(n["norm_w"]), EPS, dw["router_w"],
+                                                  dw["w_gate_up"], dw["w_down"], shape.top_k,
+                                                  shape.renorm)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(x), n["x"])
+    assert np.array_equal(_bits(r2), _bf16_add(_bits(out), n["x"]))
