@@ -17,6 +17,9 @@ HBM copy peak). The same run also times the prefill layer of the same model
 flops / time against the bf16 tensor peak for the layer, gate_up and down.
 One NVML sampler covers every timed region of the run.
 
+--tp splits one layer over the ranks instead (tensor parallelism: each rank
+a slice of the experts' intermediates, one fp32 all-reduce per step).
+
 --impl reference times the CPU oracle on the host cores instead (a baseline,
 not a target). Under torchrun every rank runs its own replica (the layer
 shards by tokens with no exchange), and rank 0 prints the line.
@@ -98,6 +101,16 @@ def max_over_ranks(x: float, ws: int, device=None) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def tp_combine(partial, ws: int):
+    """The one exchange step of the tensor-parallel split: the ranks' fp32
+    partial outputs summed over all ranks (in place; nccl on GPUs, gloo on
+    CPU)."""
+    if ws > 1:
+        import torch.distributed as dist
+        dist.all_reduce(partial, op=dist.ReduceOp.SUM)
+    return partial
 
 
 def job_tokens_per_s(T: int, ws: int, ms: float) -> float:
@@ -582,6 +595,87 @@ def _to_dev(bits, dev):
     return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
 
+def run_tp(args, shape, ws, rank, dev, mm):
+    """Tensor-parallel split of one layer over the ws ranks ("The op layer:
+    BaseOP and the layers", "Linear layers"): every rank routes the same
+    batch with the replicated router and runs the experts on its slice of
+    the intermediates (mm_moe_forward_partial), one all-reduce sums the fp32
+    partials (tp_combine, nccl), and mm_round_bf16 rounds the sum. A step is
+    the whole layer on the batch, so the job's tokens/s is T / step time
+    (strong scaling: the work is split, not repeated)."""
+    w = synthetic.make_weights(shape)
+    gu_np, dn_np = mm.tp_slice(w["w_gate_up"], w["w_down"], rank, ws)
+    router_w, gu, dn = _to_dev(w["router_w"], dev), _to_dev(gu_np, dev), _to_dev(dn_np, dev)
+    del w, gu_np, dn_np
+    hidden = _to_dev(synthetic.make_hidden(shape), dev)  # the same batch on every rank
+    bias_np = synthetic.make_router_bias(shape)
+    bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    T, H = shape.T, shape.H
+    partial = torch.empty((T, H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(h=hidden):
+        mm.mm_moe_forward_partial(h, router_w, gu, dn, shape.top_k, shape.renorm,
+                                  partial=partial, router_bias=bias)
+        tp_combine(partial, ws)
+        mm.mm_round_bf16(partial, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = args.steps or 50
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index or 0) as clk:
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, ws, dev)
+    # end to end: the batch from pinned host memory, the step, out back
+    h_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    h_host.copy_(hidden.cpu())
+    o_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    h_dev = torch.empty_like(hidden)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        step(h_dev)
+        o_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / steps, ws, dev)
+    st = mm.mm_poll_device_status()
+    if st != mm.MM_OK:
+        raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
+    pk, pk_kind = peaks()
+    flops = 2 * T * shape.E * H + 2 * T * shape.top_k * 3 * H * shape.I
+    line = {"metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": ws,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded normals, bf16; random-init weights of the named shape)",
+            "config": {"workload": shape.name, "T": T, "H": H, "E": shape.E,
+                       "top_k": shape.top_k, "I": shape.I, "I_per_rank": shape.I // ws,
+                       "renorm": shape.renorm, "parallelism": f"tp{ws}",
+                       "allreduce_bytes_per_step": T * H * 4},
+            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12,
+                         "peak": pk["bf16_tflops"] * ws, "unit": "TFLOP/s",
+                         "frac": flops / (ms * 1e-3) / 1e12 / (pk["bf16_tflops"] * ws),
+                         "peak_kind": f"{pk_kind} bf16_tflops (burst) x {ws} GPUs",
+                         "kernel": "whole step (layer on the slice, all-reduce, rounding)",
+                         "traffic": None},
+            "e2e": {"value": T / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
+                    "d2h_bytes_per_step": T * H * 2},
+            # the layer's launches, mm_round_bf16 in place of the rounding pass
+            "gpu_launches": kernel_launches(shape) * steps, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -601,6 +695,10 @@ def main():
                     help="time mm_moe_forward_add_norm_residual: the residual add + RMSNorm "
                          "step before the layer, the layer, and the residual add after it, "
                          "in one call")
+    ap.add_argument("--tp", action="store_true",
+                    help="tensor-parallel split of one layer over the ranks (each rank a slice "
+                         "of the experts' intermediates, one fp32 all-reduce per step) instead "
+                         "of one replica per rank")
     ap.add_argument("--dense", action="store_true",
                     help="time mm_gated_mlp: a dense SwiGLU MLP of H x k*I on the workload's "
                          "tokens (the same flops per token as the MoE layer's experts)")
@@ -631,6 +729,13 @@ def main():
     torch.cuda.set_device(dev)
     if args.dense:
         run_dense(args, shape, ws, rank, dev, mm)
+        return
+    if args.tp:
+        run_tp(args, shape, ws, rank, dev, mm)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
         return
     if args.add_norm and synthetic.make_router_bias(shape) is not None:
         raise SystemExit("--add-norm takes no router bias (the Zipf sweep has one)")

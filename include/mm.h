@@ -230,6 +230,40 @@ enum {
 int mm_moe_workspace_layout(int T, int H, int E, int I, int top_k, int64_t* layout);
 
 /*
+ * The layer split over W GPUs by tensor parallelism ("The op layer: BaseOP
+ * and the layers", "Linear layers": gate_up is a merged column-parallel
+ * linear, down a row-parallel linear followed by an all-reduce, the router
+ * a replicated linear). Rank r holds, for every expert, the intermediate
+ * slice [i0, i0 + I_slice): the gate rows [i0, i0 + I_slice) and the up rows
+ * [I + i0, I + i0 + I_slice) of w_gate_up, stored together as
+ * w_gate_up_slice [E, 2*I_slice, H] (gate slice first), and the columns
+ * [i0, i0 + I_slice) of w_down, stored as w_down_slice [E, H, I_slice].
+ * SiLU(gate) * up is elementwise over the intermediates, so the layer is the
+ * sum over the slices of
+ *   partial[t,:] = sum_j w[t,j] * W_down_slice[e_j] (silu(g_slice) * u_slice)
+ * which this call writes, in fp32 and unrounded, to partial [T,H] (caller-
+ * owned, overwritten). The routing comes from the replicated router and is
+ * the same on every rank. The caller sums the W partials (one all-reduce)
+ * and rounds the sum once with mm_round_bf16. Arguments as
+ * mm_moe_forward_ex with I = I_slice (a multiple of 64); partial replaces
+ * out. The fp32 sum of a rank's own experts' contributions has no fixed
+ * order (atomic adds), as in mm_moe_forward.
+ */
+int mm_moe_forward_partial(const uint16_t* hidden, const uint16_t* router_w,
+                           const float* router_bias, const uint16_t* w_gate_up_slice,
+                           const uint16_t* w_down_slice, int T, int H, int E, int I_slice,
+                           int top_k, int renorm, float* partial, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * out[i] = bf16(in[i]) (round to nearest even) for i < n: the rounding of
+ * the all-reduced partials of mm_moe_forward_partial. n % 4 == 0 (else
+ * MM_ERR_UNSUPPORTED); in fp32 and out bf16 are device pointers, 16-byte
+ * aligned.
+ */
+int mm_round_bf16(const float* in, uint16_t* out, int64_t n, void* stream);
+
+/*
  * The dense SwiGLU MLP, through the same grouped-GEMM kernels: out =
  * down_proj(silu(gate_proj(x)) * up_proj(x)) for every token ("模型与权重加载",
  * GatedMLP; Qwen3 dense layers, and the MoE model's mlp_only_layers named in

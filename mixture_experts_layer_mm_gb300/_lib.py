@@ -41,6 +41,8 @@ SIGNATURES = {
     "mm_moe_forward_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "mm_moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
                                      _P]),
+    "mm_moe_forward_partial": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mm_round_bf16": (_I, [_P, _P, _I64, _P]),
     "mm_gated_mlp": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "mm_gated_mlp_workspace_size": (_I64, [_I, _I, _I]),
     "mm_add_rmsnorm": (_I, [_P, _P, _P, ctypes.c_float, _I, _I, _P, _P]),
@@ -250,6 +252,59 @@ def mm_moe_forward(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool
                                    T, H, E, I, top_k, int(bool(renorm)),
                                    _ptr(out, torch.bfloat16, "out"), ws_ptr, ws_bytes,
                                    _stream(stream)), "mm_moe_forward_ex")
+    return out
+
+
+def tp_slice(w_gate_up, w_down, rank: int, world: int):
+    """The expert weights rank `rank` of `world` holds under tensor
+    parallelism: gate rows [i0, i0 + I/world) and the same up rows of every
+    expert, as one [E, 2*I/world, H] tensor (gate slice first), and the same
+    columns of w_down, [E, H, I/world]. Weight preparation (done once, like
+    the loader's sharding), for torch tensors or numpy arrays."""
+    E, twoI, H = w_gate_up.shape
+    I = twoI // 2
+    if world < 1 or I % world != 0:
+        raise ValueError(f"I={I} does not split into {world} equal slices")
+    il = I // world
+    i0 = rank * il
+    gate, up = w_gate_up[:, i0:i0 + il, :], w_gate_up[:, I + i0:I + i0 + il, :]
+    if isinstance(w_gate_up, torch.Tensor):
+        return torch.cat([gate, up], dim=1).contiguous(), w_down[:, :, i0:i0 + il].contiguous()
+    import numpy as np
+    return (np.ascontiguousarray(np.concatenate([gate, up], axis=1)),
+            np.ascontiguousarray(w_down[:, :, i0:i0 + il]))
+
+
+def mm_moe_forward_partial(hidden, router_w, w_gate_up_slice, w_down_slice, top_k: int,
+                           renorm: bool, partial=None, router_bias=None, workspace=None,
+                           stream=None):
+    """The layer on one tensor-parallel slice of the experts' intermediates
+    (see tp_slice): returns this rank's unrounded fp32 contribution [T, H]."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    I = w_down_slice.shape[2]
+    if partial is None:
+        partial = torch.empty((T, H), dtype=torch.float32, device=hidden.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().mm_moe_forward_partial(_ptr(hidden, torch.bfloat16, "hidden"),
+                                        _ptr(router_w, torch.bfloat16, "router_w"),
+                                        _ptr(router_bias, torch.float32, "router_bias"),
+                                        _ptr(w_gate_up_slice, torch.bfloat16, "w_gate_up_slice"),
+                                        _ptr(w_down_slice, torch.bfloat16, "w_down_slice"),
+                                        T, H, E, I, top_k, int(bool(renorm)),
+                                        _ptr(partial, torch.float32, "partial"), ws_ptr, ws_bytes,
+                                        _stream(stream)), "mm_moe_forward_partial")
+    return partial
+
+
+def mm_round_bf16(x, out=None, stream=None):
+    """bf16 rounding (to nearest even) of an fp32 tensor, on the GPU."""
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _check(lib().mm_round_bf16(_ptr(x, torch.float32, "x"), _ptr(out, torch.bfloat16, "out"),
+                               x.numel(), _stream(stream)), "mm_round_bf16")
     return out
 
 

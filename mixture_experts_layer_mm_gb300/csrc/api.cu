@@ -269,8 +269,12 @@ struct NormIn {
 int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* router_bias,
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
-                 cudaStream_t st, cudaEvent_t const* ev, const NormIn* norm = nullptr) {
+                 cudaStream_t st, cudaEvent_t const* ev, const NormIn* norm = nullptr,
+                 float* partial = nullptr) {
   if (norm != nullptr) hidden = norm->x;  // for the checks below
+  // With `partial` the layer stops before the rounding: the down GEMM adds
+  // into partial (fp32, zeroed by the gate_up kernel) and out is not used.
+  if (partial != nullptr) out = reinterpret_cast<uint16_t*>(partial);
   int rc = check_route_shape(T, H, E, top_k);
   if (rc != MM_OK) return rc;
   if (I <= 0) return MM_ERR_INVALID_ARG;
@@ -305,7 +309,7 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
   int32_t* counts = at<int32_t>(ws, L.counts);
   int32_t* scratch = at<int32_t>(ws, L.scratch);
   uint16_t* act = at<uint16_t>(ws, L.act);
-  float* acc = at<float>(ws, L.acc);
+  float* acc = partial != nullptr ? partial : at<float>(ws, L.acc);
   const long long nacc = (long long)T * H;
   auto mark = [&](int i) { return ev == nullptr || cudaEventRecord(ev[i], st) == cudaSuccess; };
 
@@ -369,6 +373,7 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
     return MM_ERR_CUDA;
   // The rounding of the sum, and with a residual output the add that follows
   // the layer, in one pass.
+  if (partial != nullptr) return MM_OK;  // the caller sums the ranks' partials and rounds
   const uint16_t* res_in = nullptr;
   uint16_t* res_out = nullptr;
   if (norm != nullptr && norm->res_out != nullptr) {
@@ -403,6 +408,30 @@ int mm_moe_forward_profiled(const uint16_t* hidden, const uint16_t* router_w,
   return forward_impl(hidden, router_w, router_bias, w_gate_up, w_down, T, H, E, I, top_k, renorm,
                       out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
                       reinterpret_cast<cudaEvent_t const*>(events));
+}
+
+int mm_moe_forward_partial(const uint16_t* hidden, const uint16_t* router_w,
+                           const float* router_bias, const uint16_t* w_gate_up_slice,
+                           const uint16_t* w_down_slice, int T, int H, int E, int I_slice,
+                           int top_k, int renorm, float* partial, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (T > 0 && partial == nullptr) return MM_ERR_INVALID_ARG;
+  return forward_impl(hidden, router_w, router_bias, w_gate_up_slice, w_down_slice, T, H, E,
+                      I_slice, top_k, renorm, nullptr, workspace, workspace_bytes,
+                      static_cast<cudaStream_t>(stream), nullptr, nullptr, partial);
+}
+
+int mm_round_bf16(const float* in, uint16_t* out, int64_t n, void* stream) {
+  if (n < 0) return MM_ERR_INVALID_ARG;
+  if (n % 4 != 0) return MM_ERR_UNSUPPORTED;
+  if (n == 0) return MM_OK;
+  if (!in || !out || !aligned16(in) || !aligned16(out)) return MM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState* s = nullptr;
+  int rc = device_state(&s);
+  if (rc != MM_OK) return rc;
+  return cuda_status(
+      launch_finalize(in, out, (long long)n, s->sms, false, static_cast<cudaStream_t>(stream)));
 }
 
 int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w, const uint16_t* w_gate_up,

@@ -160,6 +160,21 @@ def test_moe_block_residual_host_checks(lib):
                                               8, 64, 2, 1, None, None, None) == mm.MM_OK
 
 
+def test_tp_host_checks(lib):
+    L = mm.lib()
+    # the partial output is required; I_slice % 64; T == 0 is a no-op
+    assert L.mm_moe_forward_partial(16, 16, None, 16, 16, 4, 64, 8, 64, 2, 1, None, None, 0,
+                                    None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_moe_forward_partial(16, 16, None, 16, 16, 4, 64, 8, 96, 2, 1, 16, None, 0,
+                                    None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_moe_forward_partial(None, None, None, None, None, 0, 64, 8, 64, 2, 1, None, None,
+                                    0, None) == mm.MM_OK
+    assert L.mm_round_bf16(16, 16, 6, None) == mm.MM_ERR_UNSUPPORTED
+    assert L.mm_round_bf16(16, 16, -4, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_round_bf16(8, 16, 4, None) == mm.MM_ERR_INVALID_ARG
+    assert L.mm_round_bf16(None, None, 0, None) == mm.MM_OK
+
+
 def test_binding_raises_without_library(monkeypatch, tmp_path):
     import mixture_experts_layer_mm_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)
