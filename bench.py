@@ -215,6 +215,15 @@ def tensor_regime(shape) -> bool:
     return shape.T * shape.top_k > 64 * shape.E
 
 
+def decode_fused(shape) -> bool:
+    """Whether mm_moe_forward runs this shape's layer as its single
+    cooperative launch (batches of at most 16 tokens whose shape that launch
+    takes: T*k <= 512, E <= 256, H % 256 == 0 and H <= 2048, I % 128 == 0 and
+    I <= 1024)."""
+    return (1 <= shape.T <= 16 and shape.T * shape.top_k <= 512 and shape.E <= 256
+            and shape.H % 256 == 0 and shape.H <= 2048 and shape.I % 128 == 0 and shape.I <= 1024)
+
+
 def kernel_launches(shape, add_norm: bool = False) -> int:
     """Kernels one layer call launches for this shape (the launch sequence of
     the library's forward): route (which also groups when T <= 64), the
@@ -225,6 +234,8 @@ def kernel_launches(shape, add_norm: bool = False) -> int:
     (which also adds the residual after the layer in the add-norm mode); plus
     the add + RMSNorm kernel in front when add_norm."""
     T, E, k = shape.T, shape.E, shape.top_k
+    if decode_fused(shape):  # one launch for the whole layer
+        return 1 + (1 if add_norm else 0)
     fused_align = T <= 64 and T * k <= 8192
     single_align = T <= 1024 and T * k <= 8192
     router_counts = T > 2048 and E <= 128
@@ -423,6 +434,10 @@ def roofline(shape, work, stage_ms, ms, pk, pk_kind):
     against the bf16 burst peak; both fractions are in the object."""
     dom = "gate_up"
     dom_ms = stage_ms[dom]
+    if decode_fused(shape):
+        # the single-launch layer: its one kernel moves all of the layer's
+        # bytes (its time is reported as the gate_up stage)
+        dom = "layer"
     bw = work[dom]["bytes"] / (dom_ms * 1e-3) / 1e9
     tf = work[dom]["flops"] / (dom_ms * 1e-3) / 1e12
     if tensor_regime(shape):
@@ -435,7 +450,9 @@ def roofline(shape, work, stage_ms, ms, pk, pk_kind):
     roof["frac_hbm"] = bw / pk["hbm_gbs"]
     roof["frac_tensor"] = tf / pk["bf16_tflops"]
     roof["intensity_flop_per_byte"] = work[dom]["flops"] / work[dom]["bytes"]
-    roof["kernel"] = f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
+    roof["kernel"] = (f"moe_decode_kernel, whole layer ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
+                      if dom == "layer" else
+                      f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)")
     roof["traffic"] = load_traffic(shape.name, dom)
     dn_ms = stage_ms["down"]
     roof["down"] = {"frac_hbm": work["down"]["bytes"] / (dn_ms * 1e-3) / 1e9 / pk["hbm_gbs"],

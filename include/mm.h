@@ -171,6 +171,12 @@ int mm_grouped_gemm(int mode, const void* A, const uint16_t* B, void* C,
  * per-device workspace (grown on demand with cudaMalloc, which synchronises
  * the device the first time a larger size is needed); calls on one device
  * must therefore not overlap. T == 0 is a no-op.
+ *
+ * Batches of at most 16 tokens whose shape the single-launch layer takes
+ * (see mm_moe_forward_single_launch) run as that one launch; other batches
+ * run as a chain of kernels (router, grouping, gate_up, down, rounding).
+ * Both give the same routing and grouping and the same result within the
+ * rounding of the fp32 accumulation order.
  */
 int mm_moe_forward(const uint16_t* hidden, const uint16_t* router_w,
                    const uint16_t* w_gate_up, const uint16_t* w_down,
@@ -373,6 +379,46 @@ int mm_poll_device_status(void* stream);
  * Nothing faults or hangs, and the context stays usable.
  */
 int mm_selftest_wait_timeout(void* stream);
+
+/*
+ * The MoE layer for a small batch in one cooperative launch (one CTA per
+ * SM), for T <= 64, T*top_k <= 512, E <= 256, H a multiple of 256 up to 2048
+ * and I a multiple of 128 up to 1024 (otherwise MM_ERR_UNSUPPORTED; T == 0 is
+ * a no-op). Same arguments, outputs and workspace (mm_moe_workspace_size,
+ * with the routing and grouping left at mm_moe_workspace_layout's offsets)
+ * as mm_moe_forward_ex. Every CTA computes its share of the router logits;
+ * after a grid-wide wait every CTA finishes all tokens' routing (softmax
+ * over all experts, top-k, weights) and groups them by expert itself; the
+ * selected experts' weights then stream through shared memory for gate_up
+ * (+ SiLU*up) and down (weighted, added up in fp32), with grid-wide waits
+ * before down and before the rounding ("mini-sglang guide, chapter 7",
+ * paragraph on moe/fused.py: the fused MoE as a single kernel call). Every
+ * grid-wide wait is bounded: after about a second it records MM_ERR_TIMEOUT
+ * in the device status word (mm_poll_device_status) and returns.
+ * mm_moe_forward takes this path by itself for T <= 16.
+ */
+int mm_moe_forward_single_launch(const uint16_t* hidden, const uint16_t* router_w,
+                                 const float* router_bias, const uint16_t* w_gate_up,
+                                 const uint16_t* w_down, int T, int H, int E, int I, int top_k,
+                                 int renorm, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Self-test of the single-launch small-batch layer's grid-wide waits (no
+ * counterpart on the pages). Runs mm_moe_forward_single_launch on the given
+ * inputs (its shape limits apply; otherwise MM_ERR_UNSUPPORTED), with one
+ * flag set by
+ * the host: CTA 0 does not arrive at grid barrier `barrier` (0: after the
+ * router logits, 1: after gate_up, 2: after down). Every CTA's bounded wait
+ * at that barrier runs out after about a second, records MM_ERR_TIMEOUT in
+ * the device status word and returns (the weight-streaming warp first waits
+ * for its copies in flight). `out` is left undefined. barrier outside 0..2:
+ * MM_ERR_INVALID_ARG. Nothing faults or hangs, and the context stays usable.
+ */
+int mm_selftest_layer_barrier_timeout(const uint16_t* hidden, const uint16_t* router_w,
+                                      const uint16_t* w_gate_up, const uint16_t* w_down, int T,
+                                      int H, int E, int I, int top_k, int renorm, int barrier,
+                                      uint16_t* out, void* stream);
 
 /* Frees the internal workspaces of every device. Not thread-safe with calls in flight. */
 void mm_shutdown(void);

@@ -11,8 +11,8 @@ from ._lib import (  # noqa: F401
     MM_OK, PROFILE_STAGES, MMError, SIGNATURES, lib, mm_add_rmsnorm, mm_align,
     mm_align_capacity, mm_align_noalloc, mm_gated_mlp, mm_gated_mlp_workspace_size,
     mm_grouped_gemm, mm_moe_forward, mm_moe_forward_add_norm, mm_moe_forward_add_norm_residual,
-    mm_moe_forward_partial, mm_moe_forward_profiled, mm_round_bf16, tp_slice,
+    mm_moe_forward_partial, mm_moe_forward_profiled, mm_moe_forward_single_launch, mm_round_bf16, tp_slice,
     mm_moe_workspace_layout, mm_moe_workspace_size, forward_routing, WS_LAYOUT_FIELDS,
-    mm_poll_device_status, mm_route, mm_selftest_wait_timeout,
+    mm_poll_device_status, mm_route, mm_selftest_wait_timeout, mm_selftest_layer_barrier_timeout,
     mm_shutdown, status_string,
 )

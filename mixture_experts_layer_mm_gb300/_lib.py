@@ -42,6 +42,8 @@ SIGNATURES = {
     "mm_moe_forward_profiled": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P,
                                      _P]),
     "mm_moe_forward_partial": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "mm_moe_forward_single_launch": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ,
+                                          _P]),
     "mm_round_bf16": (_I, [_P, _P, _I64, _P]),
     "mm_gated_mlp": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "mm_gated_mlp_workspace_size": (_I64, [_I, _I, _I]),
@@ -52,6 +54,8 @@ SIGNATURES = {
                                               _I, _I, _I, _P, _P, _P]),
     "mm_poll_device_status": (_I, [_P]),
     "mm_selftest_wait_timeout": (_I, [_P]),
+    "mm_selftest_layer_barrier_timeout": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                                               _P]),
     "mm_shutdown": (None, []),
 }
 
@@ -255,6 +259,27 @@ def mm_moe_forward(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool
     return out
 
 
+def mm_moe_forward_single_launch(hidden, router_w, w_gate_up, w_down, top_k: int, renorm: bool,
+                                 out=None, router_bias=None, workspace=None, stream=None):
+    """The whole MoE layer in one cooperative launch (small batches; see
+    include/mm.h for the shapes it takes); returns out [T, H] bf16."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace, torch.uint8, "workspace"), workspace.numel()
+    _check(lib().mm_moe_forward_single_launch(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(router_w, torch.bfloat16, "router_w"),
+        _ptr(router_bias, torch.float32, "router_bias"),
+        _ptr(w_gate_up, torch.bfloat16, "w_gate_up"), _ptr(w_down, torch.bfloat16, "w_down"),
+        T, H, E, I, top_k, int(bool(renorm)), _ptr(out, torch.bfloat16, "out"), ws_ptr, ws_bytes,
+        _stream(stream)), "mm_moe_forward_single_launch")
+    return out
+
+
 def tp_slice(w_gate_up, w_down, rank: int, world: int):
     """The expert weights rank `rank` of `world` holds under tensor
     parallelism: gate rows [i0, i0 + I/world) and the same up rows of every
@@ -424,6 +449,24 @@ def mm_poll_device_status(stream=None) -> int:
 def mm_selftest_wait_timeout(stream=None) -> None:
     """Launches the kernel whose bounded wait must time out (see include/mm.h)."""
     _check(lib().mm_selftest_wait_timeout(_stream(stream)), "mm_selftest_wait_timeout")
+
+
+def mm_selftest_layer_barrier_timeout(hidden, router_w, w_gate_up, w_down, top_k: int,
+                                      renorm: bool, barrier: int, out=None, stream=None):
+    """Runs the single-launch small-batch layer with CTA 0 absent from grid
+    barrier `barrier` (see include/mm.h); every CTA's wait there runs out.
+    Returns out (undefined contents)."""
+    T, H = hidden.shape
+    E = router_w.shape[0]
+    I = w_down.shape[2]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=hidden.device)
+    _check(lib().mm_selftest_layer_barrier_timeout(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(router_w, torch.bfloat16, "router_w"),
+        _ptr(w_gate_up, torch.bfloat16, "w_gate_up"), _ptr(w_down, torch.bfloat16, "w_down"),
+        T, H, E, I, top_k, int(bool(renorm)), barrier, _ptr(out, torch.bfloat16, "out"),
+        _stream(stream)), "mm_selftest_layer_barrier_timeout")
+    return out
 
 
 def mm_shutdown() -> None:

@@ -83,9 +83,12 @@ int check_route_shape(int T, int H, int E, int top_k) {
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct ForwardLayout {
-  size_t normed, ids, w, sorted, offsets, counts, scratch, xs, act, acc, total;
+  size_t normed, ids, w, sorted, offsets, counts, scratch, xs, act, acc, logits, flags,
+      total;
   long long capacity;
   bool rows_in_order;  // token rows are copied into segment order before gate_up
+  bool single_ok;      // the single-launch small-batch layer (decode.cu) can run
+  bool decode;         // ... and mm_moe_forward chooses it
 };
 
 // gather_rows: whether a gate_up with many rows per expert reads a copy of
@@ -120,6 +123,13 @@ ForwardLayout forward_layout(int T, int H, int E, int I, int k, bool gather_rows
   L.xs = take(L.rows_in_order ? (size_t)L.capacity * H * 2 : 0);
   L.act = take((size_t)L.capacity * I * 2);
   L.acc = take((size_t)T * H * 4);
+  // The single-launch layer of small batches: router logits and the flags
+  // of its grid barriers (reserved wherever it can run, so that one
+  // workspace size serves mm_moe_forward and mm_moe_forward_single_launch).
+  L.single_ok = gather_rows && decode_supported(T, H, E, I, k);
+  L.decode = L.single_ok && decode_preferred(T, H, E, I, k);
+  L.logits = take(L.single_ok ? (size_t)T * E * 4 : 0);
+  L.flags = take(L.single_ok ? (size_t)decode_flag_slots() * 8 : 0);
   L.total = off;
   return L;
 }
@@ -270,7 +280,8 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
                  const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H, int E, int I,
                  int top_k, int renorm, uint16_t* out, void* workspace, size_t workspace_bytes,
                  cudaStream_t st, cudaEvent_t const* ev, const NormIn* norm = nullptr,
-                 float* partial = nullptr) {
+                 float* partial = nullptr, bool force_single = false,
+                 int absent_barrier = -1) {
   if (norm != nullptr) hidden = norm->x;  // for the checks below
   // With `partial` the layer stops before the rounding: the down GEMM adds
   // into partial (fp32, zeroed by the gate_up kernel) and out is not used.
@@ -290,6 +301,8 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
     return MM_ERR_INVALID_ARG;
   const ForwardLayout L = forward_layout(T, H, E, I, top_k, true, norm != nullptr);
   if (L.capacity >= (1LL << 31)) return MM_ERR_UNSUPPORTED;
+  if ((force_single || absent_barrier >= 0) && !L.single_ok) return MM_ERR_UNSUPPORTED;
+  const bool single = L.decode || force_single || absent_barrier >= 0;
   if (workspace != nullptr) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MM_ERR_INVALID_ARG;
     if (workspace_bytes < L.total) return MM_ERR_NO_MEMORY;
@@ -320,6 +333,26 @@ int forward_impl(const uint16_t* hidden, const uint16_t* router_w, const float* 
                            false, st) != cudaSuccess)
       return MM_ERR_CUDA;
     hidden = normed;
+  }
+  if (single) {
+    // One cooperative launch for the whole layer (decode.cu). For the stage
+    // events its time is the gate_up stage; the other stages are empty.
+    const DecodeBuffers b = {at<float>(ws, L.logits), ids, w, sorted, offsets, counts,
+                             L.capacity, act, acc, at<unsigned long long>(ws, L.flags)};
+    const uint16_t* res_in = nullptr;
+    uint16_t* res_out = nullptr;
+    if (partial == nullptr && norm != nullptr && norm->res_out != nullptr) {
+      res_in = norm->residual != nullptr ? norm->residual : norm->x;
+      res_out = norm->res_out;
+    }
+    if (!mark(1) || !mark(2)) return MM_ERR_CUDA;
+    if (launch_moe_decode(hidden, router_w, router_bias, w_gate_up, w_down, T, H, E, I, top_k,
+                          renorm, b, partial != nullptr ? nullptr : out, res_in, res_out, s->sms,
+                          s->status, st, absent_barrier >= 0 ? 0 : -1,
+                          absent_barrier) != cudaSuccess)
+      return MM_ERR_CUDA;
+    if (!mark(3) || !mark(4) || !mark(5)) return MM_ERR_CUDA;
+    return MM_OK;
   }
   const AlignOut fa = {sorted, offsets, counts, kForwardBlockM, L.capacity, s->status};
   const bool fused = route_fuses_align(T, top_k);
@@ -419,6 +452,26 @@ int mm_moe_forward_partial(const uint16_t* hidden, const uint16_t* router_w,
   return forward_impl(hidden, router_w, router_bias, w_gate_up_slice, w_down_slice, T, H, E,
                       I_slice, top_k, renorm, nullptr, workspace, workspace_bytes,
                       static_cast<cudaStream_t>(stream), nullptr, nullptr, partial);
+}
+
+int mm_selftest_layer_barrier_timeout(const uint16_t* hidden, const uint16_t* router_w,
+                                      const uint16_t* w_gate_up, const uint16_t* w_down, int T,
+                                      int H, int E, int I, int top_k, int renorm, int barrier,
+                                      uint16_t* out, void* stream) {
+  if (barrier < 0 || barrier > 2) return MM_ERR_INVALID_ARG;
+  return forward_impl(hidden, router_w, nullptr, w_gate_up, w_down, T, H, E, I, top_k, renorm, out,
+                      nullptr, 0, static_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr,
+                      true, barrier);
+}
+
+int mm_moe_forward_single_launch(const uint16_t* hidden, const uint16_t* router_w,
+                                 const float* router_bias, const uint16_t* w_gate_up,
+                                 const uint16_t* w_down, int T, int H, int E, int I, int top_k,
+                                 int renorm, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  return forward_impl(hidden, router_w, router_bias, w_gate_up, w_down, T, H, E, I, top_k, renorm,
+                      out, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), nullptr,
+                      nullptr, nullptr, true);
 }
 
 int mm_round_bf16(const float* in, uint16_t* out, int64_t n, void* stream) {

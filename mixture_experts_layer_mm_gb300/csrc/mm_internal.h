@@ -193,6 +193,39 @@ cudaError_t launch_finalize(const float* acc, uint16_t* out, long long n, int nu
                             bool after_prev, cudaStream_t st, const uint16_t* res_in = nullptr,
                             uint16_t* res_out = nullptr);
 
+// The single-launch layer for small batches (decode.cu): whether it can run
+// this shape, whether mm_moe_forward chooses it for this shape (where it
+// was measured faster than the kernel chain), the flag words its grid
+// barriers need (per workspace), and the launcher. Its workspace regions: logits [T, E] fp32, the routing and the
+// grouping (as the multi-kernel path), act [T*k, I] bf16, acc [T, H] fp32
+// (the layer's sum, or a caller's fp32 partial), flags [decode_flag_slots]
+// uint64.
+bool decode_supported(int T, int H, int E, int I, int top_k);
+bool decode_preferred(int T, int H, int E, int I, int top_k);
+int decode_flag_slots();
+struct DecodeBuffers {
+  float* logits;
+  int32_t* ids;
+  float* w;
+  int32_t* sorted;
+  int32_t* offsets;
+  int32_t* counts;
+  long long capacity;
+  uint16_t* act;
+  float* acc;
+  unsigned long long* flags;
+};
+// out NULL: acc is the result (a tensor-parallel partial); res_out: the
+// residual add after the layer, res_out = bf16(out + res_in). absent_cta /
+// absent_barrier (self-test of the bounded grid-wide wait): that CTA does
+// not arrive at that grid barrier, so every CTA's wait there runs out.
+cudaError_t launch_moe_decode(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                              const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H,
+                              int E, int I, int top_k, int renorm, const DecodeBuffers& b,
+                              uint16_t* out, const uint16_t* res_in, uint16_t* res_out,
+                              int num_sms, unsigned* err, cudaStream_t st, int absent_cta = -1,
+                              int absent_barrier = -1);
+
 // residual' = bf16(x + residual) in place (residual NULL: x is the residual),
 // normed = rmsnorm(residual', weight, eps) [T, H] bf16. H % 8 == 0.
 cudaError_t launch_add_rmsnorm(const uint16_t* x, uint16_t* residual, const uint16_t* weight,

@@ -83,12 +83,19 @@ def test_roofline_axis_follows_the_regime():
 
 def test_kernel_launches_follow_the_launch_sequence():
     # decode (T=64): route with the grouping fused, gate_up, down, finalize;
-    # prefill (T=4096): tensor-core route, grouping + row copy, gate_up, down,
-    # finalize (the kernels an ncu launch list shows per pass)
+    # up to 16 tokens: the single-launch layer; prefill (T=4096): tensor-core
+    # route, grouping + row copy, gate_up, down, finalize (the kernels an ncu
+    # launch list shows per pass)
     assert bench.kernel_launches(S.DECODE) == 4
+    assert bench.kernel_launches(S.SWEEP.with_T(1)) == 1
+    assert bench.kernel_launches(S.SWEEP.with_T(8)) == 1
+    assert bench.kernel_launches(S.SWEEP.with_T(32)) == 4
     assert bench.kernel_launches(S.PREFILL) == 5
     assert bench.kernel_launches(S.LARGE) == 5
     assert bench.kernel_launches(S.DECODE, add_norm=True) == 5
+    assert bench.kernel_launches(S.SWEEP.with_T(8), add_norm=True) == 2
+    # shapes the single launch does not take (H % 256 != 0) use the chain
+    assert bench.kernel_launches(dataclasses.replace(S.SWEEP, T=8, H=192)) == 4
     # one-block grouping; count + place + a separate row copy; E % 4 != 0
     assert bench.kernel_launches(S.SWEEP.with_T(512)) == 5
     assert bench.kernel_launches(S.SWEEP.with_T(2048)) == 7

@@ -8,7 +8,9 @@ row); the routing and grouping are still compared on the whole batch.
 The forward runs with a caller workspace, and the routing and grouping
 compared here are the ones the forward itself computed and used (read from
 that workspace at the offsets mm_moe_workspace_layout gives), whichever
-kernels it chose for the batch size: the grouping fused into the router
+kernels it chose for the batch size: the single launch (T <= 16 where its
+shape limits allow, and mm_moe_forward_single_launch up to T = 64, which
+routes and groups inside every CTA), the grouping fused into the router
 (T <= 64), the one-block grouping (T <= 1024), count + place (up to 2048
 tokens, or more than 128 experts), and the grouping from the tensor-core
 router's per-tile counts (above 2048 tokens), with the token-row copy in the
@@ -56,16 +58,18 @@ def _inputs(shape: MoEShape):
     return d, _WEIGHTS[key]["dev"]
 
 
-def _run(d, dev_w, k, renorm):
-    """One forward with a caller workspace; returns out and the routing and
-    grouping the forward left in that workspace."""
+def _run(d, dev_w, k, renorm, fn=None):
+    """One forward (mm_moe_forward, or fn with the same arguments) with a
+    caller workspace; returns out and the routing and grouping the forward
+    left in that workspace."""
+    fn = fn or mm.mm_moe_forward
     hidden = dev_bf16(d["hidden"])
     T, H = hidden.shape
     E, I = dev_w["router_w"].shape[0], dev_w["w_down"].shape[2]
     bias = None if d["router_bias"] is None else f32_dev(d["router_bias"])
     ws = torch.empty(mm.mm_moe_workspace_size(T, H, E, I, k), dtype=torch.uint8, device="cuda")
-    out = mm.mm_moe_forward(hidden, dev_w["router_w"], dev_w["w_gate_up"], dev_w["w_down"], k,
-                            renorm, router_bias=bias, workspace=ws)
+    out = fn(hidden, dev_w["router_w"], dev_w["w_gate_up"], dev_w["w_down"], k, renorm,
+             router_bias=bias, workspace=ws)
     torch.cuda.synchronize()
     assert mm.mm_poll_device_status() == mm.MM_OK
     r = mm.forward_routing(ws, T, H, E, I, k)
@@ -155,6 +159,67 @@ def test_forward_shapes(T, H, E, k, I, renorm):
     dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
     out, r = _run(d, dw, k, renorm)
     _check(d, k, renorm, out, r)
+
+
+# Shapes that mm_moe_forward_single_launch takes (T <= 64, T*k <= 512,
+# H % 256 == 0 and H <= 2048, I % 128 == 0 and I <= 1024): one expert and one
+# token; k = 1 with E not a power of two; every expert on every token (50
+# tokens per expert: two passes of token groups over each weight slot); 256
+# experts (the widest router finish) with T*k = 512; the largest I; K slices
+# of three 32-column steps with E = 40; three experts holding up to 64 tokens;
+# the decode workload itself (T = 64, its full size).
+@pytest.mark.parametrize("T,H,E,k,I,renorm", [
+    (1, 256, 1, 1, 128, True),
+    (7, 256, 6, 1, 128, True),
+    (50, 512, 8, 8, 256, False),
+    (64, 256, 256, 8, 128, True),
+    (16, 512, 4, 2, 1024, True),
+    (33, 768, 40, 5, 384, True),
+    (64, 256, 3, 2, 128, False),
+])
+def test_forward_single_launch_shapes(T, H, E, k, I, renorm):
+    d = random_small_inputs(T + 5 * E, T, H, E, I, w_std=0.08, bias=(E % 2 == 0))
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    out, r = _run(d, dw, k, renorm, fn=mm.mm_moe_forward_single_launch)
+    _check(d, k, renorm, out, r)
+
+
+def test_forward_single_launch_decode_workload():
+    d, dw = _inputs(DECODE)
+    out, r = _run(d, dw, DECODE.top_k, DECODE.renorm, fn=mm.mm_moe_forward_single_launch)
+    _check(d, DECODE.top_k, DECODE.renorm, out, r)
+
+
+def test_forward_single_launch_rejects_other_shapes():
+    T, H, E, k, I = 8, 192, 8, 2, 128  # H % 256 != 0
+    d = random_small_inputs(3, T, H, E, I, w_std=0.08)
+    dw = {n: dev_bf16(d[n]) for n in ("hidden", "router_w", "w_gate_up", "w_down")}
+    with pytest.raises(mm.MMError) as ei:
+        mm.mm_moe_forward_single_launch(dw["hidden"], dw["router_w"], dw["w_gate_up"],
+                                        dw["w_down"], k, True)
+    assert ei.value.code == mm.MM_ERR_UNSUPPORTED
+    empty = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    d = random_small_inputs(3, 1, 256, E, I, w_std=0.08)
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    out0 = mm.mm_moe_forward_single_launch(empty, dw["router_w"], dw["w_gate_up"], dw["w_down"],
+                                           k, True)
+    assert out0.shape == (0, 256)
+
+
+def test_forward_single_launch_forced_routing():
+    # every token to experts {1, 6}: 64 tokens per expert, all in the same
+    # two experts' units
+    T, H, E, k, I = 64, 256, 8, 2, 128
+    d = random_small_inputs(19, T, H, E, I, w_std=0.08)
+    dw = {n: dev_bf16(d[n]) for n in ("router_w", "w_gate_up", "w_down")}
+    bias = np.full(E, -30.0, dtype=np.float32)
+    bias[[1, 6]] = 30.0
+    out = mm.mm_moe_forward_single_launch(dev_bf16(d["hidden"]), dw["router_w"], dw["w_gate_up"],
+                                          dw["w_down"], k, True, router_bias=f32_dev(bias))
+    ids, w, _ = O.route(d["hidden"], d["router_w"], k, True, bias)
+    assert (ids == np.array([1, 6])).all()
+    ref = O.experts_loop(d["hidden"], d["w_gate_up"], d["w_down"], ids, w)
+    assert_out_close(out.float().cpu().numpy(), ref, "forced routing, single launch")
 
 
 def test_forward_closed_forms():
