@@ -306,7 +306,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     // wait for those to land, so one warp per slot keeps all stages in flight.
     const int slot = warp == 0 ? 0 : warp - kPProd0 + 1;
     if (lane == 0 && slot < kPStages) {
-      const uint64_t pol_w = l2_policy_evict_normal();  // read by every chunk of the expert
+      // Weights: read by every chunk of the expert, so kept at normal
+      // priority when the expert has several chunks, and marked first to go
+      // when it has one (read once: then they make room for the token rows
+      // and the accumulator instead of pushing those out).
+      const uint64_t pol_w_multi = l2_policy_evict_normal();
+      const uint64_t pol_w_once = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();    // read by every m-tile of the chunk
       uint32_t use = 0;  // fills of this warp's slot so far
       int q = 0;         // K step counter of this pair, modulo the ring size
@@ -319,6 +324,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int brow = row0 + (int)rank * nh;
         const int nbox = (nh + kPBox - 1) / kPBox;
         const uint32_t bytes = kPABytes + nbox * kPBox * kPK * 2;
+        const uint64_t pol_w = P.cs[e + 1] - P.cs[e] > 1 ? pol_w_multi : pol_w_once;
         for (int kb = 0; kb < nk; ++kb) {
           const bool mine = q == slot;
           if (++q == kPStages) q = 0;
