@@ -50,8 +50,14 @@ METRIC = "MoE-layer tokens/s (Qwen3-30B-A3B shape) + % of BF16 TC / HBM roofline
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ["mixture_experts_layer_mm_gb300/csrc/gemm.cu",
-                  "mixture_experts_layer_mm_gb300/csrc/mm_device.cuh"]
+# The sources of each dominant kernel family: the single-CTA grouped GEMM
+# (decode-shaped batches), the SM-pair grouped GEMM (prefill-shaped ones) and
+# the single-launch layer (batches of at most 16 tokens).
+_CSRC = "mixture_experts_layer_mm_gb300/csrc/"
+KERNEL_SOURCES = {"gemm": [_CSRC + "gemm.cu", _CSRC + "mm_device.cuh"],
+                  "pair": [_CSRC + "gemm_pair.cu", _CSRC + "mm_device.cuh"],
+                  "single": [_CSRC + "decode.cu", _CSRC + "mm_device.cuh",
+                             _CSRC + "route_finish.cuh"]}
 
 
 def peaks():
@@ -62,11 +68,18 @@ def peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(family: str) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
+
+
+def kernel_family(shape) -> str:
+    """The kernel family that runs this shape's dominant step."""
+    if decode_fused(shape):
+        return "single"
+    return "pair" if tensor_regime(shape) else "gemm"
 
 
 def dist_info():
@@ -245,12 +258,12 @@ def kernel_launches(shape, add_norm: bool = False) -> int:
     return 4 + grouping + (1 if separate_copy else 0) + (1 if add_norm else 0)
 
 
-def load_traffic(workload: str, kernel: str):
+def load_traffic(workload: str, kernel: str, family: str):
     if not os.path.exists(TRAFFIC_FILE):
         return None
     d = json.load(open(TRAFFIC_FILE))
     ent = d.get(workload, {}).get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("family") != family or ent.get("source_hash") != kernel_source_hash(family):
         return None  # counters were taken on another version of the kernel
     return ent.get("bytes_per_launch")
 
@@ -450,10 +463,11 @@ def roofline(shape, work, stage_ms, ms, pk, pk_kind):
     roof["frac_hbm"] = bw / pk["hbm_gbs"]
     roof["frac_tensor"] = tf / pk["bf16_tflops"]
     roof["intensity_flop_per_byte"] = work[dom]["flops"] / work[dom]["bytes"]
-    roof["kernel"] = (f"moe_decode_kernel, whole layer ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
-                      if dom == "layer" else
-                      f"grouped_gemm_kernel<gate_up> ({dom_ms * 1e3:.1f} us/launch, CUDA events)")
-    roof["traffic"] = load_traffic(shape.name, dom)
+    fam = kernel_family(shape)
+    kname = {"single": "moe_decode_kernel, whole layer", "pair": "grouped_gemm_pair_kernel<gate_up>",
+             "gemm": "grouped_gemm_kernel<gate_up>"}[fam]
+    roof["kernel"] = f"{kname} ({dom_ms * 1e3:.1f} us/launch, CUDA events)"
+    roof["traffic"] = load_traffic(shape.name, dom, fam)
     dn_ms = stage_ms["down"]
     roof["down"] = {"frac_hbm": work["down"]["bytes"] / (dn_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                     "frac_tensor": work["down"]["flops"] / (dn_ms * 1e-3) / 1e12 /
