@@ -41,10 +41,11 @@
 // permutation of the step's 32 columns applied to both operands alike, so
 // the dot products are unchanged and no shuffle is needed.
 //
-// Grid barriers: each CTA writes the call's epoch (a per-launch 64-bit value)
-// into its own flag of the barrier, then polls all CTAs' flags of that
-// barrier until every one holds the epoch. Flags never need clearing (a new
-// call brings a new epoch). Every wait is bounded: after about a second a CTA
+// Grid barriers: at barrier 0 each CTA writes the call's epoch (a
+// per-launch 64-bit value) into its own flag, then polls all CTAs' flags
+// until every one holds the epoch; flags never need clearing (a new call
+// brings a new epoch). Barriers 1 and 2 count arrivals on one word each,
+// zeroed before barrier 0. Every wait is bounded: after about a second a CTA
 // records MM_ERR_TIMEOUT and leaves, the producer first waiting for the
 // copies it has in flight.
 #include <math.h>
@@ -93,7 +94,7 @@ struct DecodeArgs {
   uint16_t* out;             // [T, H] bf16, or NULL (the sum is the result)
   const uint16_t* res_in;    // residual add after the layer: res_out = bf16(out + res_in)
   uint16_t* res_out;
-  unsigned long long* flags; // [kDecBarriers, kDecMaxGrid], then the work counters
+  unsigned long long* flags; // [kDecBarriers, kDecMaxGrid], then 4 u32 counters
   unsigned long long epoch;
   unsigned* err;
   int absent_cta, absent_barrier;  // self-test: that CTA skips that barrier's arrival
@@ -141,6 +142,35 @@ __device__ __forceinline__ bool grid_wait_warp(const DecodeArgs& a, int b) {
   return done;
 }
 
+// Grid barriers 1 and 2: an arrival counter each (zeroed before grid
+// barrier 0, so the zero is seen by everyone). Called by one warp after its
+// CTA's threads have arrived at a CTA barrier: lane 0 adds the CTA's arrival
+// and polls the one counter word until all CTAs have arrived (bounded). One
+// word polled by one lane per CTA keeps the L2 traffic of the wait small,
+// which matters while the weight stream keeps the memory system busy.
+__device__ __forceinline__ bool grid_count_wait(const DecodeArgs& a, unsigned* c, int b) {
+  const int lane = threadIdx.x & 31;
+  bool done = false;
+  if (lane == 0) {
+    if (!((int)blockIdx.x == a.absent_cta && b == a.absent_barrier)) {
+      __threadfence();
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(c) : "memory");
+    }
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      if (v >= gridDim.x) {
+        done = true;
+        break;
+      }
+      if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+    if (!done) atomicOr(a.err, kDevErrTimeout);
+  }
+  return __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
+}
+
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -148,6 +178,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -289,6 +323,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   __shared__ __align__(8) uint64_t full_bar[kSlots];
   __shared__ __align__(8) uint64_t empty_bar[kSlots];
   __shared__ int ok_s, nact_s;
+  __shared__ int wsum_s[kMaxExperts / 32][3];
   __shared__ volatile int abort_s;
   __shared__ volatile int ctl_s[2];
   __shared__ volatile int fill_unit[kSlots];
@@ -306,10 +341,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
     }
     fence_barrier_init();
     abort_s = 0;
-    if (blockIdx.x == 0) {  // the work counters (read after grid barrier 0)
+    if (blockIdx.x == 0) {  // the work and arrival counters (read after grid barrier 0)
       unsigned* c = reinterpret_cast<unsigned*>(a.flags + kDecBarriers * kDecMaxGrid);
       c[0] = 0u;
       c[1] = 0u;
+      c[2] = 0u;
+      c[3] = 0u;
     }
   }
   pdl_wait();
@@ -382,49 +419,55 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   __syncthreads();
   for (int i = tid; i < Tk; i += kDecThreads) atomicOr(&R.mask[R.ids[i]], 1ull << (i / a.k));
   __syncthreads();
-  if (warp == 0) {
-    // lane l owns experts [l*per, l*per + per): counts, both scans, the
-    // ascending list of selected experts
-    const int per = (a.E + 31) / 32, e0 = lane * per;
-    int c_sum = 0, p_sum = 0, n_act = 0;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
-      if (e < a.E) {
-        const int c = __popcll(R.mask[e]);
-        c_sum += c;
-        p_sum += (c + kForwardBlockM - 1) / kForwardBlockM * kForwardBlockM;
-        n_act += c > 0;
-      }
-    }
-    int ci = c_sum, pi = p_sum, ni = n_act;
+  {
+    // warp w < ceil(E/32) takes experts 32w + lane: counts, the unpadded and
+    // the padded scan and the ascending list of selected experts, as
+    // warp-local scans and then the warps' totals (conflict-free shared
+    // accesses, every warp at once)
+    const int nw = (a.E + 31) / 32;
+    const int e = warp * 32 + lane;
+    int c = 0, pc = 0, ic = 0, ip = 0;
+    unsigned bal = 0;
+    if (warp < nw) {
+      c = e < a.E ? __popcll(R.mask[e]) : 0;
+      pc = (c + kForwardBlockM - 1) / kForwardBlockM * kForwardBlockM;
+      ic = c;
+      ip = pc;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, ci, o);
-      const int v = __shfl_up_sync(0xffffffffu, pi, o);
-      const int x = __shfl_up_sync(0xffffffffu, ni, o);
-      if (lane >= o) {
-        ci += u;
-        pi += v;
-        ni += x;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, ic, o);
+        const int v = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) {
+          ic += u;
+          ip += v;
+        }
+      }
+      bal = __ballot_sync(0xffffffffu, c > 0);
+      if (lane == 31) {
+        wsum_s[warp][0] = ic;
+        wsum_s[warp][1] = ip;
+        wsum_s[warp][2] = __popc(bal);
       }
     }
-    int cr = ci - c_sum, pr = pi - p_sum, nr = ni - n_act;
-    for (int j = 0; j < per; ++j) {
-      const int e = e0 + j;
+    __syncthreads();
+    if (warp < nw) {
+      int bc = 0, bp = 0, ba = 0;
+      for (int w2 = 0; w2 < warp; ++w2) {
+        bc += wsum_s[w2][0];
+        bp += wsum_s[w2][1];
+        ba += wsum_s[w2][2];
+      }
       if (e < a.E) {
-        const int c = __popcll(R.mask[e]);
         R.cnt[e] = c;
-        R.start[e] = cr;
-        R.offp[e] = pr;
-        if (c > 0) R.act_e[nr++] = e;
-        cr += c;
-        pr += (c + kForwardBlockM - 1) / kForwardBlockM * kForwardBlockM;
+        R.start[e] = bc + ic - c;
+        R.offp[e] = bp + ip - pc;
+        if (c > 0) R.act_e[ba + __popc(bal & ((1u << lane) - 1u))] = e;
       }
-    }
-    if (lane == 31) {
-      R.start[a.E] = ci;
-      R.offp[a.E] = pi;
-      nact_s = ni;
+      if (warp == nw - 1 && lane == 31) {
+        R.start[a.E] = bc + ic;
+        R.offp[a.E] = bp + ip;
+        nact_s = ba + __popc(bal);
+      }
     }
   }
   __syncthreads();
@@ -465,6 +508,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   const uint32_t gu_rows_bytes = 8u * a.H * 2u;   // 8 gate (or up) rows
   const uint32_t dn_unit_bytes = 16u * a.I * 2u;  // 16 rows of w_down[e]
   unsigned* ctr = reinterpret_cast<unsigned*>(a.flags + kDecBarriers * kDecMaxGrid);
+
+  // L1 prefetch of the token rows that this CTA's first gate_up units read
+  // (those of the first expert of its static share, up to 32 KB), issued
+  // while the first weight copies are in flight: their first loads then hit
+  // L1 instead of waiting on L2.
+  if (sg > 0) {
+    const int e = R.act_e[(blockIdx.x * sg) / gu_per_e];
+    const int lines = a.H / 64;  // 128-byte lines of a row
+    const int n = min(R.cnt[e] * lines, 256);
+    for (int i = tid; i < n; i += kDecThreads)
+      prefetch_l1(a.hidden + (size_t)(R.slots[R.start[e] + i / lines] / a.k) * a.H +
+                  (i % lines) * 64);
+  }
 
   // ---- producer: fills the ring; fill_unit[slot] tells the consumers what
   // each fill holds (a unit or pair index, or kFillEnd: end of the phase)
@@ -516,20 +572,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
         mbar_arrive(smem_u32(&full_bar[s]));
       };
       bool go = true;
+      // Tail claims are made one step ahead: the counter's reply arrives
+      // while the producer waits for a free slot, not after it.
+      int u_dyn = G * sg + (int)atomicAdd(ctr, 1u);
       for (int u = blockIdx.x * sg; u < (int)(blockIdx.x + 1) * sg && go; ++u)
         if ((go = acquire(i))) issue_gate_up(u), ++i;
-      while (go) {
-        const int u = G * sg + (int)atomicAdd(ctr, 1u);
-        if (u >= Ug) break;
-        if ((go = acquire(i))) issue_gate_up(u), ++i;
+      while (go && u_dyn < Ug) {
+        const int u_next = G * sg + (int)atomicAdd(ctr, 1u);
+        if ((go = acquire(i))) issue_gate_up(u_dyn), ++i;
+        u_dyn = u_next;
       }
+      int pr_dyn = G * sd + (int)atomicAdd(ctr + 1, 1u);
       if (go && (go = acquire(i))) mark_end(), ++i;
       for (int pr = blockIdx.x * sd; pr < (int)(blockIdx.x + 1) * sd && go; ++pr)
         if ((go = acquire(i))) issue_down(pr), ++i;
-      while (go) {
-        const int pr = G * sd + (int)atomicAdd(ctr + 1, 1u);
-        if (pr >= Pd) break;
-        if ((go = acquire(i))) issue_down(pr), ++i;
+      while (go && pr_dyn < Pd) {
+        const int pr_next = G * sd + (int)atomicAdd(ctr + 1, 1u);
+        if ((go = acquire(i))) issue_down(pr_dyn), ++i;
+        pr_dyn = pr_next;
       }
       if (go && (go = acquire(i))) mark_end(), ++i;
       // Every copy lands before the CTA can exit.
@@ -630,7 +690,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   // ---- barrier 1: every act row is complete
   consumer_bar();
   if (warp == 0) {
-    const bool ok = grid_wait_warp(a, 1);
+    const bool ok = grid_count_wait(a, ctr + 2, 1);
     if (lane == 0) {
       ok_s = ok ? 1 : 0;
       if (!ok) abort_s = 1;
@@ -638,6 +698,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   }
   consumer_bar();
   if (!ok_s) return;
+  // L1 prefetch of the act rows of the first expert of this CTA's static
+  // down share (written by other SMs before grid barrier 1, so none of their
+  // lines can be in this SM's L1 yet).
+  if (sd > 0) {
+    const int e = R.act_e[(2 * blockIdx.x * sd) / dn_per_e];
+    const int lines = a.I / 64;
+    const int n = min(R.cnt[e] * lines, 256);
+    for (int i = tid; i < n; i += kCW * 32)
+      prefetch_l1(a.act + (size_t)R.slots[R.start[e] + i / lines] * a.I + (i % lines) * 64);
+  }
 
   // ---- D: down; a pair of units per slot, warps 4*grp .. 4*grp+3 on unit
   // grp, warp wl of the group on columns [wl*I/4, (wl+1)*I/4)
@@ -721,7 +791,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) moe_decode_kernel(const Decode
   // ---- barrier 2: the sum is complete
   consumer_bar();
   if (warp == 0) {
-    const bool ok = grid_wait_warp(a, 2);
+    const bool ok = grid_count_wait(a, ctr + 3, 2);
     if (lane == 0) ok_s = ok ? 1 : 0;
   }
   consumer_bar();
@@ -812,8 +882,10 @@ bool decode_preferred(int T, int H, int E, int I, int top_k) {
   return T <= kDecAutoMaxT && decode_supported(T, H, E, I, top_k);
 }
 
-// The barriers' flags, then one word holding the two work counters.
-int decode_flag_slots() { return kDecBarriers * kDecMaxGrid + 1; }
+// The barriers' flags (grid barrier 0 uses its epoch flags), then two words
+// holding the two work counters and the arrival counters of grid barriers 1
+// and 2.
+int decode_flag_slots() { return kDecBarriers * kDecMaxGrid + 2; }
 
 cudaError_t launch_moe_decode(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                               const uint16_t* w_gate_up, const uint16_t* w_down, int T, int H,
