@@ -684,7 +684,20 @@ def run_tp(args, shape, ws, rank, dev, mm):
     if st != mm.MM_OK:
         raise RuntimeError(f"device status after the timed regions: {mm.status_string(st)}")
     pk, pk_kind = peaks()
-    flops = 2 * T * shape.E * H + 2 * T * shape.top_k * 3 * H * shape.I
+    ids, _ = mm.mm_route(hidden, router_w, shape.top_k, shape.renorm, router_bias=bias)
+    work = algorithmic_work(shape, ids.cpu().numpy())["layer"]
+    flops, nbytes = work["flops"], work["bytes"]
+    if tensor_regime(shape):
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12,
+                "peak": pk["bf16_tflops"] * ws, "unit": "TFLOP/s",
+                "peak_kind": f"{pk_kind} bf16_tflops (burst) x {ws} GPUs"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9,
+                "peak": pk["hbm_gbs"] * ws, "unit": "GB/s",
+                "peak_kind": f"{pk_kind} hbm_gbs (copy bandwidth) x {ws} GPUs"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = "whole step (layer on the slice, all-reduce, rounding)"
+    roof["traffic"] = None
     line = {"metric": METRIC, "value": T / (ms * 1e-3), "unit": UNIT, "n_gpus": ws,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
@@ -693,12 +706,7 @@ def run_tp(args, shape, ws, rank, dev, mm):
                        "top_k": shape.top_k, "I": shape.I, "I_per_rank": shape.I // ws,
                        "renorm": shape.renorm, "parallelism": f"tp{ws}",
                        "allreduce_bytes_per_step": T * H * 4},
-            "roofline": {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12,
-                         "peak": pk["bf16_tflops"] * ws, "unit": "TFLOP/s",
-                         "frac": flops / (ms * 1e-3) / 1e12 / (pk["bf16_tflops"] * ws),
-                         "peak_kind": f"{pk_kind} bf16_tflops (burst) x {ws} GPUs",
-                         "kernel": "whole step (layer on the slice, all-reduce, rounding)",
-                         "traffic": None},
+            "roofline": roof,
             "e2e": {"value": T / e2e_s, "unit": UNIT, "h2d_bytes_per_step": T * H * 2,
                     "d2h_bytes_per_step": T * H * 2},
             # the layer's launches, mm_round_bf16 in place of the rounding pass
