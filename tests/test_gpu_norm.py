@@ -81,7 +81,8 @@ def test_add_rmsnorm_large_values():
     assert_norm_rows_close(_bits(normed), want_n)
 
 
-@pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [TINY, DECODE.with_T(8), DECODE, PREFILL],
+                         ids=lambda s: s.name)
 def test_moe_forward_add_norm(shape):
     T, H, k = shape.T, shape.H, shape.top_k
     w = make_inputs(shape)
@@ -152,7 +153,8 @@ def _bf16_add(a_bits, b_bits):
     return O.round_bf16(O.widen_bf16(a_bits) + O.widen_bf16(b_bits))
 
 
-@pytest.mark.parametrize("shape", [TINY, DECODE, PREFILL], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [TINY, DECODE.with_T(8), DECODE, PREFILL],
+                         ids=lambda s: s.name)
 @pytest.mark.parametrize("in_place", [True, False])
 def test_moe_forward_add_norm_residual(shape, in_place):
     # DecoderLayer.forward's order: residual' = x + residual, the MoE block on

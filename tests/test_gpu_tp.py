@@ -34,7 +34,10 @@ def test_round_bf16_matches_the_oracle():
     assert np.array_equal(got.view(torch.int16).cpu().numpy().view(np.uint16), O.round_bf16(x))
 
 
-@pytest.mark.parametrize("shape", [DECODE, PREFILL], ids=lambda s: s.name)
+# T=8 takes the single-launch layer for the whole layer and for 2-way
+# slices (I/2 = 384), the kernel chain for 4-way slices (I/4 = 192 is not a
+# multiple of 128).
+@pytest.mark.parametrize("shape", [DECODE.with_T(8), DECODE, PREFILL], ids=lambda s: s.name)
 @pytest.mark.parametrize("world", [2, 4])
 def test_slices_sum_to_the_layer(shape, world):
     d = make_inputs(shape)
