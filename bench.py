@@ -550,6 +550,15 @@ class LayerRun:
                 b.record(stream)
             torch.cuda.synchronize()
             ms = sum(a.elapsed_time(b) for a, b in step_ev) / steps
+            # the same steps back to back (warm L2: the weights stay), reported
+            # beside the cold headline
+            t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for _ in range(steps):
+                self.fwd()
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            self.warm_ms = max_over_ranks(t_start.elapsed_time(t_end) / steps, ws, dev)
         else:
             t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t_start.record(stream)
@@ -841,6 +850,12 @@ def main():
                     "d2h_bytes_per_step": int(run.io_bytes)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
+    if flush:
+        line["warm"] = {"ms_per_step": run.warm_ms,
+                        "value": job_tokens_per_s(shape.T, ws, run.warm_ms), "unit": UNIT,
+                        "bytes_frac_hbm": work["layer"]["bytes"] / (run.warm_ms * 1e-3) / 1e9 /
+                        pk["hbm_gbs"],
+                        "l2": "steps back to back: the step's weights stay in L2"}
     if pre is not None:
         proof = roofline(pre.shape, pre_work, pre_stage, pre_ms, pk, pk_kind)
         line[pre.shape.name + ("+add_rmsnorm" if args.add_norm else "")] = {
