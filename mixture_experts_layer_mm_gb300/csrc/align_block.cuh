@@ -26,6 +26,10 @@ __device__ __forceinline__ void block_ballots(const int* ids_s, int T, int k, in
                                               uint32_t* bal_s, unsigned* err) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tl = warp * 32 + lane, t = tok0 + tl;
+  if (tok0 + warp * 32 >= T) {  // no token in this warp (warp-uniform): empty ballots
+    for (int e = lane; e < E; e += 32) bal_s[warp * E + e] = 0u;
+    return;
+  }
   uint32_t bits[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) bits[q] = 0;

@@ -150,6 +150,8 @@ def test_forward_zipf_sweep(T):
     # row copy follows it
     (3000, 64, 100, 8, 64, False), (5000, 128, 40, 5, 192, True),
     (12000, 64, 128, 8, 64, True), (2500, 64, 30, 4, 64, True),
+    # 32-token router tiles with a ragged last tile, wider rows
+    (4100, 256, 64, 6, 128, True),
     # more than 128 experts above 2048 tokens: the cluster router, the
     # two-launch grouping and a separate row copy
     (2600, 64, 160, 4, 64, True),

@@ -73,23 +73,28 @@ def test_route_shapes(T, H, E, k, renorm, bias):
 # Batches above 2048 tokens with at most 128 experts take the tensor-core
 # router, with 32-, 64- or 128-token tiles as T grows (up to 32 x SMs, 64 x
 # SMs, beyond): odd expert counts (rows past E of its 128-row tile), bias, no
-# renorm, k up to 32, ragged last tiles.
+# renorm, k up to 32, ragged last tiles, and wider rows (H up to 768: up to
+# 12 K steps per tile).
 @pytest.mark.parametrize("T,H,E,k,renorm,bias", [
     (65, 128, 128, 8, True, False), (4097, 64, 33, 7, True, True),
     (4500, 128, 128, 8, False, False), (5000, 192, 97, 32, True, False),
     (12001, 64, 64, 1, False, True), (20000, 64, 120, 6, True, True),
+    (4097, 256, 128, 8, True, True), (4864, 512, 97, 8, False, False),
+    (2200, 768, 128, 32, True, True), (6000, 256, 64, 6, True, True),
+    (9000, 384, 128, 8, True, False), (9728, 128, 100, 4, False, True),
 ])
 def test_route_tensor_core_shapes(T, H, E, k, renorm, bias):
     d = random_small_inputs(T + E + k, T, H, E, 64, bias=bias)
     _check_route(d["hidden"], d["router_w"], d["router_bias"], k, renorm)
 
 
-@pytest.mark.parametrize("T", [4200, 8000, 20000])
-def test_route_tensor_core_forced_ties(T):
+@pytest.mark.parametrize("T,H", [(4200, 64), (8000, 64), (20000, 64), (4200, 256), (8000, 256)])
+def test_route_tensor_core_forced_ties(T, H):
     # As below, at batch sizes that take the tensor-core router with each
-    # token-tile size: exact ties between experts held by different threads
-    # of the group that finishes a token.
-    H, E, k = 64, 128, 8
+    # token-tile size (H = 256: four times the K steps per tile): exact ties
+    # between experts held by different threads of the group that finishes a
+    # token.
+    E, k = 128, 8
     c = (np.arange(E) % 5 + 1).astype(np.float64)  # values 1..5, each ~26 times
     bias = np.log(c).astype(np.float32)
     hidden = random_small_inputs(7, T, H, E, 64)["hidden"]
