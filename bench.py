@@ -9,7 +9,8 @@ The default workload is the Qwen3-30B-A3B-shaped decode layer (T=64, H=2048,
 E=128, k=8, I=768): every step streams the selected experts' weights (about
 1.2 GB, far above the 129 MB L2) from HBM, so no L2 flush is needed. Batches
 whose step reads less than twice the L2 size (--sweep-T 1) are timed step by
-step, with an L2-sized write between steps outside the timed events.
+step, with the L2 flushed between steps (a write and a read of twice its
+size) outside the timed events.
 
 The line's value, roofline and e2e are the decode layer's (fraction of the
 HBM copy peak). The same run also times the prefill layer of the same model
@@ -58,6 +59,15 @@ KERNEL_SOURCES = {"gemm": [_CSRC + "gemm.cu", _CSRC + "mm_device.cuh"],
                   "pair": [_CSRC + "gemm_pair.cu", _CSRC + "mm_device.cuh"],
                   "single": [_CSRC + "decode.cu", _CSRC + "mm_device.cuh",
                              _CSRC + "route_finish.cuh"]}
+
+
+def flush_l2(scratch):
+    """Evicts the previous step's data from L2: a write of the scratch buffer
+    (twice the L2 size), then a read of it. The write alone left part of the
+    previous step in L2 on GB300 (a small batch ran ~6 us faster after it
+    than after a read of the same size, with 2x and 4x L2 writes alike)."""
+    flush_l2(scratch)
+    scratch.sum()
 
 
 def peaks():
@@ -354,8 +364,8 @@ def run_dense(args, shape, ws, rank, dev, mm):
     flops = 2 * T * H * 2 * I + 2 * T * I * H
     nbytes = 3 * H * I * 2 + 2 * T * H * 2
     # The weights (75 MB at H=2048, I=6144) fit in L2: a step whose bytes are
-    # under twice the L2 size is timed alone, after a write of twice the L2
-    # size outside its events, as in the layer's timing.
+    # under twice the L2 size is timed alone, after the L2 is flushed (a write
+    # and a read of twice its size) outside its events, as in the layer's timing.
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = nbytes < 2 * l2_bytes
     scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
@@ -367,7 +377,7 @@ def run_dense(args, shape, ws, rank, dev, mm):
             step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(args.steps)]
             for a, b in step_ev:
-                scratch.zero_()
+                flush_l2(scratch)
                 a.record(stream)
                 fwd()
                 b.record(stream)
@@ -394,7 +404,7 @@ def run_dense(args, shape, ws, rank, dev, mm):
     t0 = time.perf_counter()
     for _ in range(args.steps):
         if flush:  # the flush is kept out of the step's wall time
-            scratch.zero_()
+            flush_l2(scratch)
             stream.synchronize()
             t0 = time.perf_counter()
         x_dev.copy_(x_host, non_blocking=True)
@@ -427,8 +437,8 @@ def run_dense(args, shape, ws, rank, dev, mm):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded normals, bf16)",
             "config": {"workload": f"dense_gated_mlp_T{T}_H{H}_I{I}", "T": T, "H": H, "I": I,
                        "parallelism": f"replicas x{ws}",
-                       "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write "
-                              f"outside each step's events): the {3 * H * I * 2 / 1e6:.0f} MB "
+                       "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write and "
+                              f"read outside each step's events): the {3 * H * I * 2 / 1e6:.0f} MB "
                               "of weights fit in L2") if flush else
                              f"weights {3 * H * I * 2 / 1e6:.0f} MB per step, inputs larger than L2"},
             "roofline": roof,
@@ -532,8 +542,9 @@ class LayerRun:
     def measure(self, steps, ws, flush_bytes, l2_bytes, e2e=True):
         """Runs regions A, B (and C); returns ms per step, stage ms, e2e s per step."""
         mm, stream, dev = self.mm, self.stream, self.dev
-        # A step whose bytes would stay in L2 is timed alone, after a write of
-        # twice the L2 size (outside its events) evicts the previous step's data.
+        # A step whose bytes would stay in L2 is timed alone, after a write and
+        # a read of twice the L2 size (outside its events) evict the previous
+        # step's data.
         flush = flush_bytes < 2 * l2_bytes
         scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
         self.flushed = flush
@@ -544,7 +555,7 @@ class LayerRun:
             step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for _ in range(steps)]
             for a, b in step_ev:
-                scratch.zero_()
+                flush_l2(scratch)
                 a.record(stream)
                 self.fwd()
                 b.record(stream)
@@ -578,7 +589,7 @@ class LayerRun:
         torch.cuda.synchronize()
         for i in range(nb):
             if flush:
-                scratch.zero_()  # before the call's first event
+                flush_l2(scratch)  # before the call's first event
             mm.mm_moe_forward_profiled(self.hidden, self.router_w, self.w_gu, self.w_dn, sh.top_k,
                                        sh.renorm, evs[i], out=self.out, router_bias=self.bias)
         torch.cuda.synchronize()
@@ -613,7 +624,7 @@ class LayerRun:
         t0 = time.perf_counter()
         for _ in range(steps):
             if flush:  # the flush is kept out of the step's wall time
-                scratch.zero_()
+                flush_l2(scratch)
                 stream.synchronize()
                 t0 = time.perf_counter()
             h_dev.copy_(h_host, non_blocking=True)
@@ -836,8 +847,8 @@ def main():
                        "T": shape.T, "H": shape.H, "E": shape.E,
                        "top_k": shape.top_k, "I": shape.I, "renorm": shape.renorm,
                        "distinct_experts": work["D"], "parallelism": f"replicas x{ws}",
-                       "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write "
-                              "outside each step's events): the step's "
+                       "l2": (f"L2 flushed between steps (a {2 * l2_bytes / 1e6:.0f} MB write and "
+                              "read outside each step's events): the step's "
                               f"{work['layer']['bytes'] / 1e6:.0f} MB would fit in L2"
                               if flush else
                               "inputs larger than L2: each step streams the selected experts' "
