@@ -66,7 +66,7 @@ def flush_l2(scratch):
     (twice the L2 size), then a read of it. The write alone left part of the
     previous step in L2 on GB300 (a small batch ran ~6 us faster after it
     than after a read of the same size, with 2x and 4x L2 writes alike)."""
-    flush_l2(scratch)
+    scratch.zero_()
     scratch.sum()
 
 

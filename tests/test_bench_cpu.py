@@ -101,3 +101,12 @@ def test_kernel_launches_follow_the_launch_sequence():
     assert bench.kernel_launches(S.SWEEP.with_T(2048)) == 7
     odd_e = dataclasses.replace(S.PREFILL, E=30, top_k=4)
     assert bench.kernel_launches(odd_e) == 6
+
+
+def test_flush_overwrites_the_scratch_buffer():
+    # The flush between small steps writes the whole buffer and reads it back
+    # (here on a CPU tensor: the same torch calls the GPU run makes).
+    torch = pytest.importorskip("torch")
+    scratch = torch.full((1024,), 7.0)
+    bench.flush_l2(scratch)
+    assert torch.count_nonzero(scratch).item() == 0
